@@ -1,0 +1,123 @@
+"""fp8_quant_row_gb300: fused LayerNorm -> AdaLN modulate -> FP8 E4M3 row kernels for GB300.
+
+Python binding of the C ABI in include/fp8q.h. This layer only marshals arguments: it checks
+tensor dtypes/devices, allocates outputs with torch when the caller passes none, and calls
+the library on the current torch CUDA stream. Every step of the computation runs in the
+library's sm_103a kernels; there is no CPU or eager fallback.
+
+    y, q = nss_fp8(x, scale, shift, input_scale)                      # q: float8_e4m3fn
+    r, y, q = scale_residual_nss_fp8(x, residual, gate, scale, shift, input_scale, bias=b)
+    y = bias_mul_add(x, bias, gate, residual)
+    q = token_cat_fp8(attention, mlp, input_scale)
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _capi
+from ._build import build
+from ._capi import Fp8qError
+
+__all__ = ["nss_fp8", "scale_residual_nss_fp8", "bias_mul_add", "token_cat_fp8", "build",
+           "Fp8qError", "library_path"]
+
+EPS = 1e-6
+
+
+def library_path() -> str:
+    return _capi.LIB
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _bf16(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous CUDA bfloat16 tensor, got "
+                        f"{t.dtype} on {t.device} (contiguous={t.is_contiguous()})")
+    return t
+
+
+def _scale_ptr(input_scale: torch.Tensor) -> int:
+    if input_scale.dtype != torch.float32 or not input_scale.is_cuda or input_scale.numel() != 1:
+        raise TypeError("input_scale: expected a one-element float32 CUDA tensor")
+    return input_scale.data_ptr()
+
+
+def _out(out, shape, dtype, like: torch.Tensor, name: str) -> torch.Tensor:
+    if out is None:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    if out.dtype != dtype or tuple(out.shape) != tuple(shape) or not out.is_contiguous():
+        raise TypeError(f"{name}: expected contiguous {dtype} {tuple(shape)}")
+    return out
+
+
+def _rows_cols(x: torch.Tensor):
+    cols = x.shape[-1]
+    return (x.numel() // cols if cols else 0), cols
+
+
+def nss_fp8(x, scale, shift, input_scale, *, mod_rows: int = 0, eps: float = EPS, y=None,
+            q=None, stream=None):
+    """LayerNorm (no affine) -> modulate -> (bf16 y, float8_e4m3fn q). x: [..., cols]."""
+    _bf16(x, "x"), _bf16(scale, "scale"), _bf16(shift, "shift")
+    rows, cols = _rows_cols(x)
+    y = _out(y, x.shape, torch.bfloat16, x, "y")
+    q = _out(q, x.shape, torch.float8_e4m3fn, x, "q")
+    st = _capi.lib().fp8q_nss_fp8(y.data_ptr(), q.data_ptr(), x.data_ptr(), scale.data_ptr(),
+                                  shift.data_ptr(), int(mod_rows), _scale_ptr(input_scale),
+                                  rows, cols, float(eps), _stream_handle(stream))
+    _capi.check(st, "fp8q_nss_fp8")
+    return y, q
+
+
+def scale_residual_nss_fp8(x, residual, gate, scale, shift, input_scale, *, bias=None,
+                           mod_rows: int = 0, eps: float = EPS, residual_out=None, y=None,
+                           q=None, stream=None):
+    """residual_out = RN(RN(x + bias) * gate + residual); (y, q) = nss_fp8(residual_out)."""
+    for t, n in ((x, "x"), (residual, "residual"), (gate, "gate"), (scale, "scale"),
+                 (shift, "shift")):
+        _bf16(t, n)
+    if bias is not None:
+        _bf16(bias, "bias")
+    rows, cols = _rows_cols(x)
+    residual_out = _out(residual_out, x.shape, torch.bfloat16, x, "residual_out")
+    y = _out(y, x.shape, torch.bfloat16, x, "y")
+    q = _out(q, x.shape, torch.float8_e4m3fn, x, "q")
+    st = _capi.lib().fp8q_scale_residual_nss_fp8(
+        residual_out.data_ptr(), y.data_ptr(), q.data_ptr(), x.data_ptr(), residual.data_ptr(),
+        None if bias is None else bias.data_ptr(), gate.data_ptr(), scale.data_ptr(),
+        shift.data_ptr(), int(mod_rows), _scale_ptr(input_scale), rows, cols, float(eps),
+        _stream_handle(stream))
+    _capi.check(st, "fp8q_scale_residual_nss_fp8")
+    return residual_out, y, q
+
+
+def bias_mul_add(x, bias, gate, residual, *, y=None, stream=None):
+    """y = RN(RN(x + bias) * gate + residual), the last rounding single (BF16 FMA)."""
+    for t, n in ((x, "x"), (bias, "bias"), (gate, "gate"), (residual, "residual")):
+        _bf16(t, n)
+    rows, cols = _rows_cols(x)
+    y = _out(y, x.shape, torch.bfloat16, x, "y")
+    st = _capi.lib().fp8q_bias_mul_add(y.data_ptr(), x.data_ptr(), bias.data_ptr(),
+                                       gate.data_ptr(), residual.data_ptr(), rows, cols,
+                                       _stream_handle(stream))
+    _capi.check(st, "fp8q_bias_mul_add")
+    return y
+
+
+def token_cat_fp8(a, m, input_scale, *, q=None, stream=None):
+    """float8_e4m3fn q = E4M3(cat(a, m, dim=-1) * RN(1/input_scale)), no BF16 concat."""
+    _bf16(a, "a"), _bf16(m, "m")
+    rows, a_cols = _rows_cols(a)
+    m_cols = m.shape[-1]
+    if m.numel() != rows * m_cols:
+        raise TypeError("a and m must have the same number of rows")
+    q = _out(q, (*a.shape[:-1], a_cols + m_cols), torch.float8_e4m3fn, a, "q")
+    st = _capi.lib().fp8q_token_cat_fp8(q.data_ptr(), a.data_ptr(), a_cols, m.data_ptr(),
+                                        m_cols, _scale_ptr(input_scale), rows,
+                                        _stream_handle(stream))
+    _capi.check(st, "fp8q_token_cat_fp8")
+    return q

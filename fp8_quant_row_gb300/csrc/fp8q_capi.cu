@@ -1,0 +1,348 @@
+// fp8q_capi.cu -- host side of libfp8q: argument validation, device checks, launch shapes.
+//
+// Every entry point validates synchronously and returns a status before anything is
+// enqueued; it then launches exactly one kernel on the caller's stream. Nothing here
+// allocates device memory or synchronises, so the calls can be captured in CUDA graphs
+// once the per-device launch caches below are warm (first call on a device queries
+// attributes).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "fp8q.h"
+#include "elementwise_kernels.cuh"
+#include "nss_kernels.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxLnCols = 32768;
+constexpr int64_t kMaxEwCols = int64_t(1) << 30;
+
+thread_local int g_last_cuda_error = 0;
+
+struct DeviceInfo {
+  int major = 0, minor = 0, sms = 0, smem_optin = 0;
+  bool ok = false;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+
+fp8q_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = int(e);
+  return FP8Q_ERR_CUDA;
+}
+
+// Current device, checked to be compute capability 10.3.
+fp8q_status current_device(const DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return FP8Q_ERR_UNSUPPORTED;
+  std::call_once(g_dev_once[dev], [dev] {
+    DeviceInfo& d = g_dev[dev];
+    d.ok = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+           cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+           cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+           cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ==
+               cudaSuccess;
+  });
+  const DeviceInfo& d = g_dev[dev];
+  if (!d.ok) return cuda_fail(cudaErrorInvalidDevice);
+  if (d.major != 10 || d.minor != 3) return FP8Q_ERR_UNSUPPORTED;
+  *out = &d;
+  return FP8Q_OK;
+}
+
+// Resident CTAs per SM of a kernel at a dynamic shared-memory size, cached per device.
+struct OccEntry {
+  int dev;
+  const void* fn;
+  size_t smem;
+  int blocks;
+};
+OccEntry g_occ[256];
+int g_occ_n = 0;
+std::mutex g_occ_mu;
+
+fp8q_status blocks_per_sm(const void* fn, int threads, size_t smem, int* blocks) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lock(g_occ_mu);
+  for (int i = 0; i < g_occ_n; ++i)
+    if (g_occ[i].dev == dev && g_occ[i].fn == fn && g_occ[i].smem == smem) {
+      *blocks = g_occ[i].blocks;
+      return FP8Q_OK;
+    }
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  int b = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (g_occ_n < 256) g_occ[g_occ_n++] = OccEntry{dev, fn, smem, b};
+  *blocks = b;
+  return FP8Q_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  const void* p;
+  size_t bytes;
+};
+
+bool overlap(Range a, Range b) {
+  if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+bool same(Range a, Range b) { return a.p == b.p && a.bytes == b.bytes; }
+
+fp8q_status launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8Q_OK : cuda_fail(e);
+}
+
+// ------------------------------------------------------------------------------------------
+// LayerNorm family
+// ------------------------------------------------------------------------------------------
+
+template <int V, int WPR, bool RESID, bool HAS_BIAS>
+fp8q_status launch_tuned(const fp8q::NssParams& p, const DeviceInfo& dev, int64_t n_mod,
+                         cudaStream_t stream, bool* launched) {
+  using L = fp8q::TunedLayout<V, WPR, RESID>;
+  auto* fn = fp8q::nss_tuned_kernel<V, WPR, RESID, HAS_BIAS>;
+  const int slots = n_mod > 1 ? 2 : 1;
+  const size_t smem = L::smem_bytes(slots);
+  *launched = false;
+  if (smem > size_t(dev.smem_optin)) return FP8Q_OK;
+  int bps = 0;
+  fp8q_status st = blocks_per_sm(reinterpret_cast<const void*>(fn), fp8q::kNssThreads, smem, &bps);
+  if (st != FP8Q_OK) return st;
+  if (bps <= 0) return FP8Q_OK;
+  const int64_t need = (p.rows + L::kRowsPerIter - 1) / L::kRowsPerIter;
+  int64_t grid = int64_t(dev.sms) * bps;
+  if (grid > need) grid = need;
+  // A CTA's contiguous row block may touch at most two modulation rows.
+  if (p.mod_rows > 0 && n_mod > 1 && p.mod_rows < (p.rows + grid - 1) / grid) return FP8Q_OK;
+  fn<<<dim3(unsigned(grid)), dim3(fp8q::kNssThreads), smem, stream>>>(p);
+  *launched = true;
+  return launch_status();
+}
+
+template <bool RESID, bool HAS_BIAS>
+fp8q_status launch_generic(const fp8q::NssParams& p, const DeviceInfo& dev, cudaStream_t stream) {
+  auto* fn = fp8q::nss_generic_kernel<RESID, HAS_BIAS>;
+  const size_t smem = size_t(p.cols) * 2;
+  int bps = 0;
+  fp8q_status st = blocks_per_sm(reinterpret_cast<const void*>(fn), fp8q::kNssThreads, smem, &bps);
+  if (st != FP8Q_OK) return st;
+  if (bps <= 0) return cuda_fail(cudaErrorInvalidConfiguration);
+  int64_t grid = int64_t(dev.sms) * bps;
+  if (grid > p.rows) grid = p.rows;
+  fn<<<dim3(unsigned(grid)), dim3(fp8q::kNssThreads), smem, stream>>>(p);
+  return launch_status();
+}
+
+template <bool RESID, bool HAS_BIAS>
+fp8q_status dispatch_ln(const fp8q::NssParams& p, const DeviceInfo& dev, int64_t n_mod,
+                        cudaStream_t stream) {
+  bool launched = false;
+  fp8q_status st = FP8Q_OK;
+  if (p.cols == 3072)
+    st = launch_tuned<12, 1, RESID, HAS_BIAS>(p, dev, n_mod, stream, &launched);
+  else if (p.cols == 6144)
+    st = launch_tuned<12, 2, RESID, HAS_BIAS>(p, dev, n_mod, stream, &launched);
+  if (st != FP8Q_OK || launched) return st;
+  return launch_generic<RESID, HAS_BIAS>(p, dev, stream);
+}
+
+fp8q_status check_ln_shape(int64_t rows, int64_t cols, int64_t mod_rows, float eps) {
+  if (rows < 0 || mod_rows < 0) return FP8Q_ERR_SHAPE;
+  if (cols < 8 || cols > kMaxLnCols || cols % 8 != 0) return FP8Q_ERR_SHAPE;
+  if (!std::isfinite(eps) || eps < 0.0f) return FP8Q_ERR_VALUE;
+  return FP8Q_OK;
+}
+
+int64_t mod_count(int64_t rows, int64_t mod_rows) {
+  return mod_rows > 0 ? (rows + mod_rows - 1) / mod_rows : 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8q_status fp8q_nss_fp8(void* y_bf16, uint8_t* q_e4m3, const void* x_bf16,
+                         const void* scale_bf16, const void* shift_bf16, int64_t mod_rows,
+                         const float* input_scale, int64_t rows, int64_t cols, float eps,
+                         cudaStream_t stream) {
+  fp8q_status st = check_ln_shape(rows, cols, mod_rows, eps);
+  if (st != FP8Q_OK || rows == 0) return st;
+  if (!y_bf16 || !q_e4m3 || !x_bf16 || !scale_bf16 || !shift_bf16 || !input_scale)
+    return FP8Q_ERR_NULL;
+  if (!aligned16(y_bf16) || !aligned16(q_e4m3) || !aligned16(x_bf16) || !aligned16(scale_bf16) ||
+      !aligned16(shift_bf16))
+    return FP8Q_ERR_ALIGN;
+  const int64_t n_mod = mod_count(rows, mod_rows);
+  const size_t n = size_t(rows) * size_t(cols);
+  const Range y{y_bf16, n * 2}, q{q_e4m3, n}, x{x_bf16, n * 2};
+  const Range sc{scale_bf16, size_t(n_mod) * cols * 2}, sh{shift_bf16, size_t(n_mod) * cols * 2};
+  const Range is{input_scale, 4};
+  for (Range out : {y, q})
+    for (Range in : {x, sc, sh, is})
+      if (overlap(out, in)) return FP8Q_ERR_ALIAS;
+  if (overlap(y, q)) return FP8Q_ERR_ALIAS;
+  const DeviceInfo* dev = nullptr;
+  st = current_device(&dev);
+  if (st != FP8Q_OK) return st;
+  fp8q::NssParams p{};
+  p.x = static_cast<const uint16_t*>(x_bf16);
+  p.scale = static_cast<const uint16_t*>(scale_bf16);
+  p.shift = static_cast<const uint16_t*>(shift_bf16);
+  p.y = static_cast<uint16_t*>(y_bf16);
+  p.q = q_e4m3;
+  p.input_scale = input_scale;
+  p.rows = rows;
+  p.mod_rows = mod_rows;
+  p.cols = int(cols);
+  p.eps = eps;
+  return dispatch_ln<false, false>(p, *dev, n_mod, stream);
+}
+
+fp8q_status fp8q_scale_residual_nss_fp8(void* residual_out, void* y_bf16, uint8_t* q_e4m3,
+                                        const void* x_bf16, const void* residual_bf16,
+                                        const void* bias_bf16, const void* gate_bf16,
+                                        const void* scale_bf16, const void* shift_bf16,
+                                        int64_t mod_rows, const float* input_scale,
+                                        int64_t rows, int64_t cols, float eps,
+                                        cudaStream_t stream) {
+  fp8q_status st = check_ln_shape(rows, cols, mod_rows, eps);
+  if (st != FP8Q_OK || rows == 0) return st;
+  if (!residual_out || !y_bf16 || !q_e4m3 || !x_bf16 || !residual_bf16 || !gate_bf16 ||
+      !scale_bf16 || !shift_bf16 || !input_scale)
+    return FP8Q_ERR_NULL;
+  if (!aligned16(residual_out) || !aligned16(y_bf16) || !aligned16(q_e4m3) ||
+      !aligned16(x_bf16) || !aligned16(residual_bf16) || !aligned16(gate_bf16) ||
+      !aligned16(scale_bf16) || !aligned16(shift_bf16) || (bias_bf16 && !aligned16(bias_bf16)))
+    return FP8Q_ERR_ALIGN;
+  const int64_t n_mod = mod_count(rows, mod_rows);
+  const size_t n = size_t(rows) * size_t(cols);
+  const size_t mod_bytes = size_t(n_mod) * cols * 2;
+  const Range ro{residual_out, n * 2}, y{y_bf16, n * 2}, q{q_e4m3, n};
+  const Range x{x_bf16, n * 2}, res{residual_bf16, n * 2}, b{bias_bf16, size_t(cols) * 2};
+  const Range g{gate_bf16, mod_bytes}, sc{scale_bf16, mod_bytes}, sh{shift_bf16, mod_bytes};
+  const Range is{input_scale, 4};
+  for (Range out : {ro, y, q})
+    for (Range in : {x, res, b, g, sc, sh, is}) {
+      if (out.p == ro.p && same(ro, res) && in.p == res.p) continue;  // in-place residual
+      if (overlap(out, in)) return FP8Q_ERR_ALIAS;
+    }
+  if (overlap(ro, y) || overlap(ro, q) || overlap(y, q)) return FP8Q_ERR_ALIAS;
+  const DeviceInfo* dev = nullptr;
+  st = current_device(&dev);
+  if (st != FP8Q_OK) return st;
+  fp8q::NssParams p{};
+  p.x = static_cast<const uint16_t*>(x_bf16);
+  p.residual = static_cast<const uint16_t*>(residual_bf16);
+  p.bias = static_cast<const uint16_t*>(bias_bf16);
+  p.gate = static_cast<const uint16_t*>(gate_bf16);
+  p.scale = static_cast<const uint16_t*>(scale_bf16);
+  p.shift = static_cast<const uint16_t*>(shift_bf16);
+  p.residual_out = static_cast<uint16_t*>(residual_out);
+  p.y = static_cast<uint16_t*>(y_bf16);
+  p.q = q_e4m3;
+  p.input_scale = input_scale;
+  p.rows = rows;
+  p.mod_rows = mod_rows;
+  p.cols = int(cols);
+  p.eps = eps;
+  if (bias_bf16) return dispatch_ln<true, true>(p, *dev, n_mod, stream);
+  return dispatch_ln<true, false>(p, *dev, n_mod, stream);
+}
+
+fp8q_status fp8q_bias_mul_add(void* y_bf16, const void* x_bf16, const void* bias_bf16,
+                              const void* gate_bf16, const void* residual_bf16, int64_t rows,
+                              int64_t cols, cudaStream_t stream) {
+  if (rows < 0 || cols < 8 || cols % 8 != 0 || cols > kMaxEwCols) return FP8Q_ERR_SHAPE;
+  if (rows == 0) return FP8Q_OK;
+  if (!y_bf16 || !x_bf16 || !bias_bf16 || !gate_bf16 || !residual_bf16) return FP8Q_ERR_NULL;
+  if (!aligned16(y_bf16) || !aligned16(x_bf16) || !aligned16(bias_bf16) ||
+      !aligned16(gate_bf16) || !aligned16(residual_bf16))
+    return FP8Q_ERR_ALIGN;
+  const size_t n = size_t(rows) * size_t(cols);
+  const Range y{y_bf16, n * 2}, x{x_bf16, n * 2}, res{residual_bf16, n * 2};
+  const Range b{bias_bf16, size_t(cols) * 2}, g{gate_bf16, size_t(cols) * 2};
+  // Elementwise: y may be exactly x or exactly residual; partial overlaps are rejected.
+  if ((overlap(y, x) && !same(y, x)) || (overlap(y, res) && !same(y, res)) || overlap(y, b) ||
+      overlap(y, g))
+    return FP8Q_ERR_ALIAS;
+  const DeviceInfo* dev = nullptr;
+  fp8q_status st = current_device(&dev);
+  if (st != FP8Q_OK) return st;
+  const int chunks = int(cols / 8);
+  const int per_cta = fp8q::kEwThreads * fp8q::kBmaUnroll;
+  const unsigned gy = unsigned((chunks + per_cta - 1) / per_cta);
+  const unsigned gx = unsigned(rows < 0x7FFFFFFF ? rows : 0x7FFFFFFF);
+  if (gy > 65535u) return FP8Q_ERR_SHAPE;
+  fp8q::bias_mul_add_kernel<<<dim3(gx, gy), dim3(fp8q::kEwThreads), 0, stream>>>(
+      static_cast<uint16_t*>(y_bf16), static_cast<const uint16_t*>(x_bf16),
+      static_cast<const uint16_t*>(bias_bf16), static_cast<const uint16_t*>(gate_bf16),
+      static_cast<const uint16_t*>(residual_bf16), rows, int(cols));
+  return launch_status();
+}
+
+fp8q_status fp8q_token_cat_fp8(uint8_t* q_e4m3, const void* a_bf16, int64_t a_cols,
+                               const void* m_bf16, int64_t m_cols, const float* input_scale,
+                               int64_t rows, cudaStream_t stream) {
+  if (rows < 0 || a_cols < 16 || m_cols < 16 || a_cols % 16 != 0 || m_cols % 16 != 0 ||
+      a_cols + m_cols > kMaxEwCols)
+    return FP8Q_ERR_SHAPE;
+  if (rows == 0) return FP8Q_OK;
+  if (!q_e4m3 || !a_bf16 || !m_bf16 || !input_scale) return FP8Q_ERR_NULL;
+  if (!aligned16(q_e4m3) || !aligned16(a_bf16) || !aligned16(m_bf16)) return FP8Q_ERR_ALIGN;
+  const Range q{q_e4m3, size_t(rows) * size_t(a_cols + m_cols)};
+  const Range a{a_bf16, size_t(rows) * size_t(a_cols) * 2};
+  const Range m{m_bf16, size_t(rows) * size_t(m_cols) * 2};
+  const Range is{input_scale, 4};
+  if (overlap(q, a) || overlap(q, m) || overlap(q, is)) return FP8Q_ERR_ALIAS;
+  const DeviceInfo* dev = nullptr;
+  fp8q_status st = current_device(&dev);
+  if (st != FP8Q_OK) return st;
+  const int chunks = int((a_cols + m_cols) / 8);
+  const int per_cta = fp8q::kEwThreads * fp8q::kCatUnroll;
+  const unsigned gy = unsigned((chunks + per_cta - 1) / per_cta);
+  const unsigned gx = unsigned(rows < 0x7FFFFFFF ? rows : 0x7FFFFFFF);
+  if (gy > 65535u) return FP8Q_ERR_SHAPE;
+  fp8q::token_cat_fp8_kernel<<<dim3(gx, gy), dim3(fp8q::kEwThreads), 0, stream>>>(
+      q_e4m3, static_cast<const uint16_t*>(a_bf16), int(a_cols),
+      static_cast<const uint16_t*>(m_bf16), int(m_cols), input_scale, rows);
+  return launch_status();
+}
+
+const char* fp8q_status_string(int status) {
+  switch (status) {
+    case FP8Q_OK: return "ok";
+    case FP8Q_ERR_NULL: return "null pointer";
+    case FP8Q_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case FP8Q_ERR_SHAPE: return "unsupported shape";
+    case FP8Q_ERR_UNSUPPORTED: return "device is not compute capability 10.3 (GB300)";
+    case FP8Q_ERR_ALIAS: return "an output overlaps an input or another output";
+    case FP8Q_ERR_CUDA: return "CUDA runtime error";
+    case FP8Q_ERR_VALUE: return "scalar argument out of range";
+    default: return "unknown status";
+  }
+}
+
+int fp8q_last_cuda_error(void) { return g_last_cuda_error; }
+
+int fp8q_version(void) { return 0x000100; }
+
+}  // extern "C"

@@ -1,0 +1,220 @@
+// fp8q_device.cuh -- device-side building blocks of the fused row kernels (sm_103a).
+//
+// Packed-type conversions are single PTX instructions:
+//   cvt.rn.bf16x2.f32           two fp32 -> two bf16, round-to-nearest-even
+//   cvt.rn.satfinite.e4m3x2.f32 two fp32 -> two E4M3 codes, RNE, saturating to +-448
+//   fma.rn.bf16x2               two single-rounded bf16 fused multiply-adds
+// Double-float ("dd") helpers carry the LayerNorm statistics at ~2^-45 relative precision
+// with fp32 arithmetic only (GB300's fp64 rate is far too low for a per-element path). They
+// follow the error-free transformations of Knuth (TwoSum), Dekker (FastTwoSum) and the
+// FMA-based TwoProduct; all operations use explicit _rn intrinsics so the compiler can
+// neither contract nor reassociate them.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8q {
+
+// ------------------------------------------------------------------------------------------
+// bf16 / e4m3 packing
+// ------------------------------------------------------------------------------------------
+
+// Low / high bf16 of a packed pair as fp32 (exact: bf16 is the top half of a binary32).
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Pack two fp32 into bf16x2 with RNE: `lo` goes to bits 0..15, `hi` to bits 16..31.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 -> two E4M3 codes (RNE, satfinite): `lo` in bits 0..7, `hi` in bits 8..15.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Elementwise single-rounded bf16 FMA on packed pairs: a * b + c.
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// Streaming 16-byte global accesses (data touched once).
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }
+__device__ __forceinline__ void st_stream(uint2* p, uint2 v) { __stcs(p, v); }
+
+// ------------------------------------------------------------------------------------------
+// double-float arithmetic
+// ------------------------------------------------------------------------------------------
+
+struct dd {
+  float hi, lo;
+};
+
+// Knuth TwoSum: s = RN(a + b), e exact error (any magnitudes).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bv = __fsub_rn(s, a);
+  const float av = __fsub_rn(s, bv);
+  e = __fadd_rn(__fsub_rn(a, av), __fsub_rn(b, bv));
+}
+
+// Dekker FastTwoSum: exact when |a| >= |b| (or a == 0).
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  e = __fsub_rn(b, __fsub_rn(s, a));
+}
+
+// TwoProduct with FMA: p = RN(a * b), e exact error.
+__device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
+  p = __fmul_rn(a, b);
+  e = __fmaf_rn(a, b, -p);
+}
+
+__device__ __forceinline__ dd dd_add(dd a, dd b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  dd r;
+  fast_two_sum(s, e, r.hi, r.lo);
+  return r;
+}
+
+__device__ __forceinline__ dd dd_neg(dd a) { return dd{-a.hi, -a.lo}; }
+
+// a / c for a small exact float c (the row width): q1 = RN(a.hi / c), exact remainder,
+// second quotient digit.
+__device__ __forceinline__ dd dd_div_f(dd a, float c) {
+  const float q1 = __fdiv_rn(a.hi, c);
+  float p, pe;
+  two_prod(q1, c, p, pe);
+  const float rem = __fadd_rn(__fsub_rn(__fsub_rn(a.hi, p), pe), a.lo);
+  const float q2 = __fdiv_rn(rem, c);
+  dd r;
+  fast_two_sum(q1, q2, r.hi, r.lo);
+  return r;
+}
+
+__device__ __forceinline__ dd dd_sqr(dd a) {
+  float p, pe;
+  two_prod(a.hi, a.hi, p, pe);
+  pe = __fmaf_rn(__fmul_rn(2.0f, a.hi), a.lo, pe);
+  dd r;
+  fast_two_sum(p, pe, r.hi, r.lo);
+  return r;
+}
+
+// 1 / sqrt(w) for w > 0 as a double-float: correctly rounded fp32 seed, then one Newton
+// step r <- r0 + r0 * (1 - w r0^2) / 2 evaluated with the residual 1 - w r0^2 in exact
+// arithmetic up to the w.lo term (relative error ~2^-46).
+__device__ __forceinline__ dd dd_rsqrt(dd w) {
+  const float r0 = __frsqrt_rn(w.hi);
+  float a, b;
+  two_prod(r0, r0, a, b);          // r0^2 = a + b exactly
+  float p, pe;
+  two_prod(w.hi, a, p, pe);        // w.hi * a = p + pe exactly
+  const float rest = __fadd_rn(pe, __fmaf_rn(w.hi, b, __fmul_rn(w.lo, a)));
+  const float h = __fsub_rn(__fsub_rn(1.0f, p), rest);  // 1 - p is exact (p ~ 1)
+  const float corr = __fmul_rn(__fmul_rn(r0, h), 0.5f);
+  dd r;
+  fast_two_sum(r0, corr, r.hi, r.lo);
+  return r;
+}
+
+// Row constants of the LayerNorm, from exact-ish row sums sum(x) and sum(x^2).
+struct RowConst {
+  float mu_hi;     // mean, high part
+  float mu_lo;     // mean, low part
+  float r_hi;      // 1/sqrt(var + eps), high part
+  float r_lo;      // low part
+  float c;         // RN(-mu_lo * r_hi): folds the low part of the mean into one FMA
+  float t_small;   // |t| below this goes to the exact path (absolute error dominates there)
+};
+
+__device__ __forceinline__ RowConst row_constants(dd sum, dd sumsq, float cols, float eps) {
+  const dd mu = dd_div_f(sum, cols);
+  const dd e2 = dd_div_f(sumsq, cols);
+  dd var = dd_add(e2, dd_neg(dd_sqr(mu)));
+  if (!(var.hi > 0.0f)) var = dd{0.0f, 0.0f};  // exact zero for constant rows; no negatives
+  float ws, we;
+  two_sum(var.hi, eps, ws, we);
+  dd w;
+  fast_two_sum(ws, __fadd_rn(we, var.lo), w.hi, w.lo);
+  const dd r = dd_rsqrt(w);
+  RowConst k;
+  k.mu_hi = mu.hi;
+  k.mu_lo = mu.lo;
+  k.r_hi = r.hi;
+  k.r_lo = r.lo;
+  k.c = -__fmul_rn(mu.lo, r.hi);
+  // Absolute error of the fast path is below ~2^-45 * r * |mu|; require |t| >= 2^-20 r |mu|
+  // so that it stays under a quarter of an fp32 ulp of t.
+  k.t_small = __fmul_rn(__fmul_rn(fabsf(mu.hi), r.hi), 0x1p-20f);
+  return k;
+}
+
+// ------------------------------------------------------------------------------------------
+// normalised value n = RN_bf16((x - mu) * rstd)
+// ------------------------------------------------------------------------------------------
+
+// Fast path: t = RN(RN(x - mu_hi) * r_hi + c). Its error is below 4 fp32 ulps of t plus the
+// absolute term bounded through t_small; the bf16 rounding of t is therefore certain unless
+// the low 16 bits of t are within kGuard of the midpoint pattern 0x8000, or |t| < t_small.
+constexpr uint32_t kGuard = 8;
+constexpr uint32_t kGuardAdd = ((kGuard - 0x8000u) & 0xFFFFu) << 16;
+constexpr uint32_t kGuardMax = (2u * kGuard) << 16;
+
+__device__ __forceinline__ float norm_fast(float x, const RowConst& k) {
+  return __fmaf_rn(__fsub_rn(x, k.mu_hi), k.r_hi, k.c);
+}
+
+__device__ __forceinline__ bool norm_uncertain(float t, const RowConst& k) {
+  const uint32_t g = (__float_as_uint(t) << 16) + kGuardAdd;
+  return (g <= kGuardMax) | (fabsf(t) < k.t_small);
+}
+
+// Exact path: t = (x - mu) * r in double-float, then RN_bf16 of (t_hi + t_lo): t_hi decides
+// unless it sits exactly on a bf16 midpoint, where the sign of t_lo breaks the tie (t_lo is
+// below half an fp32 ulp, far below half a bf16 quantum). Returns the bf16 bits of n.
+__device__ __forceinline__ uint32_t norm_exact_bits(float x, const RowConst& k) {
+  float s, e;
+  two_sum(x, -k.mu_hi, s, e);
+  float d_hi, d_lo;
+  two_sum(s, __fsub_rn(e, k.mu_lo), d_hi, d_lo);
+  float p, pe;
+  two_prod(d_hi, k.r_hi, p, pe);
+  pe = __fadd_rn(pe, __fmaf_rn(d_hi, k.r_lo, __fmul_rn(d_lo, k.r_hi)));
+  float t_hi, t_lo;
+  fast_two_sum(p, pe, t_hi, t_lo);
+  const uint32_t u = __float_as_uint(t_hi);
+  if ((u & 0xFFFFu) == 0x8000u && t_lo != 0.0f) {
+    const bool mag_up = (t_lo > 0.0f) == (t_hi > 0.0f);
+    return (u >> 16) + (mag_up ? 1u : 0u);
+  }
+  return pack_bf16x2(t_hi, 0.0f) & 0xFFFFu;
+}
+
+// ------------------------------------------------------------------------------------------
+// per-element epilogue: modulate, quantise
+// ------------------------------------------------------------------------------------------
+
+// y = RN_bf16(fma(n, one_plus_scale, shift)) for two elements (n given as fp32 values of
+// bf16 numbers); returns the packed bf16 pair.
+__device__ __forceinline__ uint32_t modulate2(float n0, float n1, float ops0, float ops1,
+                                              float sh0, float sh1) {
+  return pack_bf16x2(__fmaf_rn(n0, ops0, sh0), __fmaf_rn(n1, ops1, sh1));
+}
+
+// q for a packed bf16 pair y: E4M3(RN(y * inv)); returns 16 bits (two codes).
+__device__ __forceinline__ uint32_t quant2(uint32_t ypair, float inv) {
+  return pack_e4m3x2(__fmul_rn(bf_lo(ypair), inv), __fmul_rn(bf_hi(ypair), inv));
+}
+
+}  // namespace fp8q

@@ -1,0 +1,152 @@
+/*
+ * fp8q.h -- C ABI of libfp8q: fused row kernels for the DiT-block prologue on GB300 (sm_103a).
+ *
+ *   nss_fp8                 LayerNorm (no affine) -> AdaLN modulate -> dual output:
+ *                           BF16 y and its static per-tensor FP8 E4M3 quantisation q.
+ *   scale_residual_nss_fp8  gated residual update (optional input bias), then nss_fp8.
+ *   bias_mul_add            deferred output-bias epilogue y = (x + bias) * gate + residual.
+ *   token_cat_fp8           E4M3 quantisation of the row concat [a | m] without a BF16 concat.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers to row-major, contiguous arrays on the current
+ *     CUDA device. bf16 tensors are raw bfloat16 bits (uint16); E4M3 tensors are raw
+ *     e4m3fn codes (uint8: no infinities, 0x7F/0xFF NaN, largest finite 448).
+ *   - The caller owns every buffer. The library allocates nothing, never synchronises and
+ *     only enqueues work on `stream` (0 = the legacy default stream). Outputs are complete
+ *     when that stream reaches the launch.
+ *   - Every tensor pointer must be 16-byte aligned (FP8Q_ERR_ALIGN otherwise).
+ *   - rows == 0 returns FP8Q_OK without touching any pointer or launching anything.
+ *   - Argument errors are reported synchronously, before any launch, with a status code; a
+ *     failed launch returns FP8Q_ERR_CUDA (fp8q_last_cuda_error() gives the cudaError_t).
+ *   - input_scale is a device pointer to ONE fp32 value; it must be finite and > 0. That
+ *     precondition is not checked (checking would need a device-to-host copy and a sync).
+ *     The kernels use inv = RN_fp32(1 / *input_scale), a correctly rounded fp32 division.
+ *   - Encode rule: q = E4M3(RN_fp32(v * inv)), saturating (|.| >= 448 -> +-448),
+ *     round-to-nearest-even; NaN gives 0x7F.
+ *   - Only compute capability 10.3 (GB300) is supported (FP8Q_ERR_UNSUPPORTED otherwise).
+ *
+ * Sources (page title and section):
+ *   [QWEN-NQ]   "sglang #37156 - Qwen-Image FP8 norm + activation-quant fusion":
+ *               implementation breakdown items 1-2, key source snippets (norm_scale_shift.cuh,
+ *               norm_scale_shift_jit.py).
+ *   [QWEN-BIAS] "sglang #37116 - Qwen-Image output-bias deferral": implementation breakdown
+ *               item 3, key source snippets (bias_mul_add_kernel), review highlights.
+ *   [FLUX-FP8]  "sglang #37162 - FLUX.2 FP8 LayerNorm/quant/QKV fusions": implementation
+ *               breakdown items 2 and 4, key source snippets (_token_cat_fp8_kernel).
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fp8q_status {
+    FP8Q_OK = 0,
+    FP8Q_ERR_NULL = 1,        /* a required pointer is NULL (with rows > 0)                   */
+    FP8Q_ERR_ALIGN = 2,       /* a tensor pointer is not 16-byte aligned                      */
+    FP8Q_ERR_SHAPE = 3,       /* rows < 0, unsupported cols / a_cols / m_cols, mod_rows < 0   */
+    FP8Q_ERR_UNSUPPORTED = 4, /* current device is not compute capability 10.3                */
+    FP8Q_ERR_ALIAS = 5,       /* an output overlaps an input or another output (see per call) */
+    FP8Q_ERR_CUDA = 6,        /* a CUDA runtime query or the kernel launch failed             */
+    FP8Q_ERR_VALUE = 7        /* a scalar argument is out of range (eps < 0 or not finite)    */
+} fp8q_status;
+
+/*
+ * LayerNorm -> modulate -> dual BF16 + E4M3 output, one row at a time [QWEN-NQ].
+ *
+ *   mu = mean(x[r,:]), var = mean((x[r,:] - mu)^2)       (population variance, no affine)
+ *   n  = RN_bf16((x - mu) / sqrt(var + eps))             (normalised value, BF16-rounded)
+ *   y  = RN_bf16(fma_fp32(n, RN_fp32(1 + scale[m,:]), shift[m,:]))     m = r / mod_rows
+ *   q  = E4M3(RN_fp32(y * inv))
+ *
+ *   y_bf16      out  [rows, cols] bf16
+ *   q_e4m3      out  [rows, cols] e4m3 codes
+ *   x_bf16      in   [rows, cols] bf16
+ *   scale_bf16  in   [n_mod, cols] bf16, n_mod = mod_rows ? ceil(rows / mod_rows) : 1
+ *   shift_bf16  in   [n_mod, cols] bf16
+ *   mod_rows    rows that share one scale/shift row (per-sample modulation); 0 = one row
+ *               broadcast over all rows
+ *   input_scale in   device pointer to one fp32 (finite, > 0)
+ *   cols        multiple of 8, 8 <= cols <= 32768 (3072 and 6144 take the tuned path)
+ *   eps         >= 0 and finite (1e-6 on the pages)
+ *   Aliasing: no output may overlap any input or the other output (FP8Q_ERR_ALIAS).
+ *   Statistics are exact to about 2^-45 relative; each normalised value is rounded to BF16
+ *   as the exact value would be, except when that value lies within ~2^-44 relative of a
+ *   BF16 rounding midpoint.
+ */
+fp8q_status fp8q_nss_fp8(void* y_bf16, uint8_t* q_e4m3, const void* x_bf16,
+                         const void* scale_bf16, const void* shift_bf16, int64_t mod_rows,
+                         const float* input_scale, int64_t rows, int64_t cols, float eps,
+                         cudaStream_t stream);
+
+/*
+ * Gated scale-residual with optional input bias, then nss_fp8 on the updated residual
+ * [QWEN-NQ implementation breakdown item 1; QWEN-BIAS implementation breakdown item 3].
+ *
+ *   xb           = bias ? RN_bf16(x + bias) : x
+ *   residual_out = RN_bf16(xb * gate[m,:] + residual)     (single rounding, BF16 FMA)
+ *   (y, q)       = nss_fp8(residual_out, scale, shift, ...)
+ *
+ *   residual_out out [rows, cols] bf16; may be exactly the residual buffer (in-place update)
+ *   y, q         out as in fp8q_nss_fp8
+ *   x, residual  in  [rows, cols] bf16
+ *   bias         in  [cols] bf16 or NULL (no input bias)
+ *   gate, scale, shift in [n_mod, cols] bf16 (m = r / mod_rows as above)
+ *   Aliasing: residual_out may equal residual exactly; every other overlap is rejected.
+ */
+fp8q_status fp8q_scale_residual_nss_fp8(void* residual_out, void* y_bf16, uint8_t* q_e4m3,
+                                        const void* x_bf16, const void* residual_bf16,
+                                        const void* bias_bf16, const void* gate_bf16,
+                                        const void* scale_bf16, const void* shift_bf16,
+                                        int64_t mod_rows, const float* input_scale,
+                                        int64_t rows, int64_t cols, float eps,
+                                        cudaStream_t stream);
+
+/*
+ * Deferred output-bias epilogue [QWEN-BIAS key source snippets]:
+ *   y = RN_bf16(RN_bf16(x + bias) * gate + residual), the second rounding single (BF16 FMA).
+ *
+ *   y        out [rows, cols] bf16; may equal x or residual exactly (elementwise in place)
+ *   x        in  [rows, cols] bf16
+ *   bias     in  [cols] bf16
+ *   gate     in  [cols] bf16
+ *   residual in  [rows, cols] bf16
+ *   cols     multiple of 8, >= 8
+ */
+fp8q_status fp8q_bias_mul_add(void* y_bf16, const void* x_bf16, const void* bias_bf16,
+                              const void* gate_bf16, const void* residual_bf16, int64_t rows,
+                              int64_t cols, cudaStream_t stream);
+
+/*
+ * Token concat -> E4M3 [FLUX-FP8 implementation breakdown item 4, key source snippets]:
+ *   q[r, c] = E4M3(RN_fp32(v * inv)),  v = a[r, c] (c < a_cols) else m[r, c - a_cols].
+ * The BF16 concat [a | m] is never materialised.
+ *
+ *   q       out [rows, a_cols + m_cols] e4m3 codes (row stride a_cols + m_cols)
+ *   a       in  [rows, a_cols] bf16 (attention output, 6144 wide on FLUX.2)
+ *   m       in  [rows, m_cols] bf16 (SwiGLU output, 18432 wide on FLUX.2)
+ *   a_cols, m_cols  multiples of 16, >= 16
+ *   Aliasing: q may not overlap a or m.
+ */
+fp8q_status fp8q_token_cat_fp8(uint8_t* q_e4m3, const void* a_bf16, int64_t a_cols,
+                               const void* m_bf16, int64_t m_cols, const float* input_scale,
+                               int64_t rows, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char* fp8q_status_string(int status);
+
+/* cudaError_t of the last FP8Q_ERR_CUDA returned on the calling host thread (0 if none). */
+int fp8q_last_cuda_error(void);
+
+/* Library ABI version: 0x00MMmmpp. */
+int fp8q_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

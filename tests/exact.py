@@ -161,3 +161,17 @@ def rnb_of_quotient(d: Fraction, w: Fraction) -> int:
         else:
             pick = lo if bits[lo] % 2 == 0 else hi
     return (0x8000 if neg else 0) | bits[pick]
+
+
+@lru_cache(maxsize=1)
+def bf16_product_ties():
+    """All pairs (m1, m2) of 8-bit significands (128..255) whose exact product lies exactly
+    on a midpoint between two adjacent bf16 values (integer enumeration)."""
+    out = []
+    for m1 in range(128, 256):
+        for m2 in range(128, 256):
+            p = m1 * m2
+            low = p.bit_length() - 8
+            if low > 0 and p % (1 << low) == (1 << (low - 1)):
+                out.append((m1, m2))
+    return out

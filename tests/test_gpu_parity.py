@@ -1,0 +1,322 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, element by element.
+
+Acceptance (per stage):
+  * bias_mul_add, token_cat_fp8, residual_out: bit-exact.
+  * quantise stage: q_gpu == E4M3(RN(y_gpu * inv)) bit-exact for every element (the
+    oracle's quantise applied to the GPU's own y).
+  * LayerNorm outputs: max |ulp| of y <= 1 against the oracle; q bit-exact wherever y
+    matches, at most one E4M3 code step elsewhere.
+Every output buffer is canary-guarded (no write outside it).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+MAX_Y_ULP = 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import fp8_quant_row_gb300 as fq
+    fq.build()
+    return fq
+
+
+def fq():
+    import fp8_quant_row_gb300
+    return fp8_quant_row_gb300
+
+
+def check_ln(y_gpu, q_gpu, y_ref, q_ref, input_scale, what=""):
+    d = G.bf16_ulp_diff(y_gpu, y_ref)
+    nmis = int((d != 0).sum())
+    assert d.max(initial=0) <= MAX_Y_ULP, f"{what}: y max ulp {d.max()} ({nmis} mismatches)"
+    same = d == 0
+    assert np.array_equal(q_gpu[same], q_ref[same]), f"{what}: q differs where y matches"
+    assert G.e4m3_step_diff(q_gpu[~same], q_ref[~same]).max(initial=0) <= 1, what
+    inv = oracle.recip_f32(input_scale)
+    assert np.array_equal(q_gpu, oracle.quantize_array(G.bf16_as_f32(y_gpu), inv)), \
+        f"{what}: quantise stage not bit-exact on the GPU's own y"
+    return nmis
+
+
+def run_nss(inp, input_scale, mod_rows=0, eps=1e-6):
+    x = G.dev_bf16(inp["x"])
+    rows, cols = inp["x"].shape
+    y = G.Guarded((rows, cols), torch.bfloat16)
+    q = G.Guarded((rows, cols), torch.float8_e4m3fn)
+    fq().nss_fp8(x, G.dev_bf16(inp["scale"]), G.dev_bf16(inp["shift"]), G.dev_scale(input_scale),
+                 mod_rows=mod_rows, eps=eps, y=y.tensor, q=q.tensor)
+    torch.cuda.synchronize()
+    assert y.intact() and q.intact(), "write outside an output buffer"
+    return G.host_u16(y.tensor), G.host_u8(q.tensor)
+
+
+# ------------------------------------------------------------------------------------------
+# nss_fp8
+# ------------------------------------------------------------------------------------------
+
+def test_nss_tiny_config():
+    c = W.CONFIGS["nss_tiny"]
+    inp = W.config_inputs("nss_tiny")
+    yg, qg = run_nss(inp, c["input_scale"])
+    yr, qr = oracle.nss_fp8(inp["x"], inp["scale"], inp["shift"], c["input_scale"])
+    check_ln(yg, qg, yr, qr, c["input_scale"], "nss tiny")
+
+
+@pytest.mark.parametrize("input_scale", W.QWEN_INPUT_SCALES)
+@pytest.mark.parametrize("rows", (1, 127, 1024, 4608))
+def test_nss_qwen_sweep(rows, input_scale):
+    inp = W.config_inputs("nss_qwen", rows=rows)
+    yg, qg = run_nss(inp, input_scale)
+    yr, qr = oracle.nss_fp8(inp["x"], inp["scale"], inp["shift"], input_scale)
+    n = check_ln(yg, qg, yr, qr, input_scale, f"nss qwen rows={rows} s={input_scale}")
+    assert n <= max(2, rows // 256)
+
+
+def test_nss_flux_per_sample_modulation():
+    c = W.CONFIGS["nss_flux"]
+    inp = W.config_inputs("nss_flux")
+    yg, qg = run_nss(inp, c["input_scale"], mod_rows=c["mod_rows"])
+    yr, qr = oracle.nss_fp8(inp["x"], inp["scale"], inp["shift"], c["input_scale"],
+                            mod_rows=c["mod_rows"])
+    check_ln(yg, qg, yr, qr, c["input_scale"], "nss flux")
+
+
+@pytest.mark.parametrize("rows,cols,mod_rows", [
+    (1, 8, 0), (3, 16, 0), (5, 24, 2), (7, 1000, 0), (33, 4096, 0), (2, 32768, 0),
+    (1, 3072, 0), (2, 3072, 0), (3, 3072, 1), (9, 3072, 4), (1000, 3072, 300),
+    (1, 6144, 0), (3, 6144, 0), (17, 6144, 5), (1001, 6144, 500), (300, 6144, 0),
+])
+def test_nss_shapes_and_ragged_rows(rows, cols, mod_rows):
+    n_mod = (rows + mod_rows - 1) // mod_rows if mod_rows else 1
+    inp = W.nss_inputs(rows, cols, seed=rows * 7 + cols, n_mod=n_mod, outlier_channels=cols // 100)
+    yg, qg = run_nss(inp, 0.05, mod_rows=mod_rows)
+    yr, qr = oracle.nss_fp8(inp["x"], inp["scale"], inp["shift"], 0.05, mod_rows=mod_rows)
+    check_ln(yg, qg, yr, qr, 0.05, f"shape {rows}x{cols}/{mod_rows}")
+
+
+def test_nss_degenerate_rows():
+    """Constant rows (var = 0), tiny spreads (var ~ eps), large means, huge values that
+    saturate the E4M3 encode, zero rows."""
+    cols = 3072
+    rng = np.random.default_rng(0)
+    rows = []
+    bf = lambda v: W.to_bf16_bits(torch.tensor(np.asarray(v, np.float32)))
+    rows.append(bf(np.full(cols, 0.75)))
+    rows.append(bf(np.zeros(cols)))
+    rows.append(bf(rng.standard_normal(cols) * 1e-3))
+    rows.append(bf(100.0 + rng.standard_normal(cols) * 0.01))
+    rows.append(bf(rng.standard_normal(cols) * 3e4))
+    rows.append(bf(np.where(rng.random(cols) < 0.5, -1.0, 1.0)))
+    rows.append(bf(rng.standard_normal(cols) * 1e-30))
+    x = np.stack(rows)
+    g = torch.Generator().manual_seed(1)
+    scale = W.normal_bf16((1, cols), 0.1, g)
+    shift = W.normal_bf16((1, cols), 0.1, g)
+    big_shift = W.normal_bf16((1, cols), 300.0, g)
+    for sh in (shift, big_shift):
+        for s in (0.0625, 0.0123):
+            inp = dict(x=x, scale=scale, shift=sh)
+            yg, qg = run_nss(inp, s)
+            yr, qr = oracle.nss_fp8(x, scale, sh, s)
+            check_ln(yg, qg, yr, qr, s, "degenerate")
+    # constant row: n == 0 exactly, so y == shift bitwise
+    yg, _ = run_nss(dict(x=x, scale=scale, shift=shift), 0.05)
+    assert np.array_equal(yg[0], shift[0]) and np.array_equal(yg[1], shift[0])
+
+
+def test_nss_eps_values():
+    inp = W.nss_inputs(64, 3072, seed=3)
+    for eps in (0.0, 1e-6, 1e-2):
+        yg, qg = run_nss(inp, 0.05, eps=eps)
+        yr, qr = oracle.nss_fp8(inp["x"], inp["scale"], inp["shift"], 0.05, eps=eps)
+        check_ln(yg, qg, yr, qr, 0.05, f"eps={eps}")
+
+
+# ------------------------------------------------------------------------------------------
+# scale_residual_nss_fp8 and bias_mul_add
+# ------------------------------------------------------------------------------------------
+
+def run_scale_residual(inp, input_scale, with_bias=True, in_place=False, mod_rows=0):
+    rows, cols = inp["x"].shape
+    x = G.dev_bf16(inp["x"])
+    res = G.dev_bf16(inp["residual"])
+    y = G.Guarded((rows, cols), torch.bfloat16)
+    q = G.Guarded((rows, cols), torch.float8_e4m3fn)
+    ro = None if in_place else G.Guarded((rows, cols), torch.bfloat16)
+    bias = G.dev_bf16(inp["bias"]) if with_bias else None
+    r_out, _, _ = fq().scale_residual_nss_fp8(
+        x, res, G.dev_bf16(inp["gate"]), G.dev_bf16(inp["scale"]), G.dev_bf16(inp["shift"]),
+        G.dev_scale(input_scale), bias=bias, mod_rows=mod_rows,
+        residual_out=res if in_place else ro.tensor, y=y.tensor, q=q.tensor)
+    torch.cuda.synchronize()
+    assert y.intact() and q.intact() and (in_place or ro.intact())
+    return G.host_u16(r_out), G.host_u16(y.tensor), G.host_u8(q.tensor)
+
+
+@pytest.mark.parametrize("with_bias", (True, False))
+def test_scale_residual_qwen_config(with_bias):
+    c = W.CONFIGS["scale_residual_qwen"]
+    inp = W.config_inputs("scale_residual_qwen")
+    rg, yg, qg = run_scale_residual(inp, c["input_scale"], with_bias=with_bias)
+    rr, yr, qr = oracle.scale_residual_nss_fp8(inp["x"], inp["residual"],
+                                               inp["bias"] if with_bias else None, inp["gate"],
+                                               inp["scale"], inp["shift"], c["input_scale"])
+    assert np.array_equal(rg, rr), "residual_out must be bit-exact"
+    check_ln(yg, qg, yr, qr, c["input_scale"], f"scale-residual bias={with_bias}")
+
+
+def test_scale_residual_in_place_and_shapes():
+    for rows, cols, mod_rows in ((37, 3072, 0), (20, 6144, 7), (5, 1024, 0), (3, 40, 1)):
+        n_mod = (rows + mod_rows - 1) // mod_rows if mod_rows else 1
+        inp = W.residual_inputs(rows, cols, seed=rows + cols, n_mod=n_mod)
+        rg, yg, qg = run_scale_residual(inp, 0.05, in_place=True, mod_rows=mod_rows)
+        rr, yr, qr = oracle.scale_residual_nss_fp8(inp["x"], inp["residual"], inp["bias"],
+                                                   inp["gate"], inp["scale"], inp["shift"], 0.05,
+                                                   mod_rows=mod_rows)
+        assert np.array_equal(rg, rr)
+        check_ln(yg, qg, yr, qr, 0.05, f"in-place {rows}x{cols}")
+
+
+def test_bias_mul_add_qwen_config_bit_exact():
+    inp = W.config_inputs("bias_mul_add_qwen")
+    rows, cols = inp["x"].shape
+    y = G.Guarded((rows, cols), torch.bfloat16)
+    fq().bias_mul_add(G.dev_bf16(inp["x"]), G.dev_bf16(inp["bias"]), G.dev_bf16(inp["gate"][0]),
+                      G.dev_bf16(inp["residual"]), y=y.tensor)
+    torch.cuda.synchronize()
+    assert y.intact()
+    ref = oracle.bias_mul_add(inp["x"], inp["bias"], inp["gate"][0], inp["residual"])
+    assert np.array_equal(G.host_u16(y.tensor), ref)
+
+
+def test_bias_mul_add_tie_cases_and_page_example():
+    """The page's extreme-value row, exact product ties with +/-/0 residuals, wide exponent
+    gaps, and in-place outputs."""
+    import json, os
+    ex = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                     "bias_fma_tie_example.json")))["inputs"]
+    cols = 64
+    rng = np.random.default_rng(5)
+    bf = lambda v: W.to_bf16_bits(torch.tensor(np.asarray(v, np.float32)))
+    x = bf(rng.standard_normal((4, cols)) * 2.0 ** rng.integers(-20, 20, (4, cols)))
+    r = bf(rng.standard_normal((4, cols)) * 2.0 ** rng.integers(-20, 20, (4, cols)))
+    b = bf(rng.standard_normal(cols) * 2.0 ** rng.integers(-20, 20, cols))
+    g = bf(rng.standard_normal(cols) * 2.0 ** rng.integers(-20, 20, cols))
+    x[0, 0], b[0], g[0], r[0, 0] = bf([ex["x"], ex["bias"], ex["gate"], ex["residual"]])
+    # exact ties: significand pairs whose product sits on a bf16 midpoint; the residual is
+    # zero or a tiny +- value that must break the tie
+    from tests.exact import bf16_product_ties
+    ties = bf16_product_ties()
+    for j in range(1, cols):
+        m1, m2 = ties[(j * 37) % len(ties)]
+        x[1, j] = bf((-1) ** j * m1 * 2.0 ** (j % 7 - 7))
+        b[j] = bf(0.0)
+        g[j] = bf(m2 * 2.0 ** -(j % 5 + 7))
+        r[1, j] = bf([0.0, 2.0 ** -30, -(2.0 ** -30)][j % 3])
+    ref = oracle.bias_mul_add(x, b, g, r)
+    for mode in ("fresh", "into_x", "into_residual"):
+        xd, rd = G.dev_bf16(x), G.dev_bf16(r)
+        out = {"fresh": None, "into_x": xd, "into_residual": rd}[mode]
+        y = fq().bias_mul_add(xd, G.dev_bf16(b), G.dev_bf16(g), rd, y=out)
+        torch.cuda.synchronize()
+        assert np.array_equal(G.host_u16(y), ref), mode
+    assert G.bf16_as_f32(ref[0:1, 0:1])[0, 0] == -5079040.0
+
+
+# ------------------------------------------------------------------------------------------
+# token_cat_fp8
+# ------------------------------------------------------------------------------------------
+
+def run_token_cat(a, m, s):
+    rows = a.shape[0]
+    q = G.Guarded((rows, a.shape[1] + m.shape[1]), torch.float8_e4m3fn)
+    fq().token_cat_fp8(G.dev_bf16(a), G.dev_bf16(m), G.dev_scale(s), q=q.tensor)
+    torch.cuda.synchronize()
+    assert q.intact()
+    return G.host_u8(q.tensor)
+
+
+def test_token_cat_flux_config_bit_exact():
+    c = W.CONFIGS["token_cat_flux"]
+    inp = W.config_inputs("token_cat_flux")
+    qg = run_token_cat(inp["a"], inp["m"], c["input_scale"])
+    qr = oracle.token_cat_fp8(inp["a"], inp["m"], c["input_scale"])
+    assert np.array_equal(qg, qr)
+
+
+@pytest.mark.parametrize("rows,a_cols,m_cols", [(1, 6144, 18432), (127, 6144, 18432),
+                                                (3, 16, 16), (5, 48, 80), (9, 1024, 16)])
+def test_token_cat_shapes(rows, a_cols, m_cols):
+    inp = W.token_cat_inputs(rows, a_cols, m_cols, seed=rows)
+    for s in (0.1, 0.0625, 0.4754464328):
+        assert np.array_equal(run_token_cat(inp["a"], inp["m"], s),
+                              oracle.token_cat_fp8(inp["a"], inp["m"], s))
+
+
+def test_token_cat_special_values():
+    """+-Inf saturate, NaN encodes 0x7F, -0 and bf16 subnormals, exact E4M3 midpoints."""
+    specials = np.array([0x7F80, 0xFF80, 0x7FC0, 0x8000, 0x0000, 0x0001, 0x8001, 0x007F,
+                         0x7F7F, 0xFF7F, 0x3F80, 0xBF80], np.uint16)
+    mids = []
+    for c in range(0x7E):
+        v = np.float32((oracle.e4m3_decode(c) + oracle.e4m3_decode(c + 1)) / 2)
+        mids.append(int(W.to_bf16_bits(torch.tensor([v]))[0]))
+    vals = np.concatenate([specials, np.array(mids, np.uint16), np.array(mids, np.uint16) | 0x8000])
+    vals = np.resize(vals, 2 * 256).reshape(2, 256)
+    q = run_token_cat(vals[:, :128].copy(), vals[:, 128:].copy(), 1.0)
+    ref = oracle.token_cat_fp8(vals[:, :128], vals[:, 128:], 1.0)
+    assert np.array_equal(q, ref)
+
+
+# ------------------------------------------------------------------------------------------
+# boundary behaviour on the device
+# ------------------------------------------------------------------------------------------
+
+def test_rows_zero_launches_nothing_and_returns_ok():
+    L = fq()._capi.lib()
+    assert L.fp8q_nss_fp8(None, None, None, None, None, 0, None, 0, 3072, 1e-6, None) == 0
+    assert L.fp8q_token_cat_fp8(None, None, 16, None, 16, None, 0, None) == 0
+
+
+def test_errors_are_reported_before_launch():
+    L = fq()._capi.lib()
+    x = torch.zeros(4, 3072, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    q = torch.empty(4, 3072, dtype=torch.uint8, device="cuda")
+    sc = torch.zeros(3072, dtype=torch.bfloat16, device="cuda")
+    s = G.dev_scale(1.0)
+    args = lambda **kw: [kw.get("y", y.data_ptr()), kw.get("q", q.data_ptr()),
+                         kw.get("x", x.data_ptr()), sc.data_ptr(), sc.data_ptr(), 0, s.data_ptr(),
+                         kw.get("rows", 4), kw.get("cols", 3072), kw.get("eps", 1e-6), None]
+    assert L.fp8q_nss_fp8(*args()) == 0
+    assert L.fp8q_nss_fp8(*args(x=x.data_ptr() + 2)) == 2
+    assert L.fp8q_nss_fp8(*args(y=x.data_ptr())) == 5
+    assert L.fp8q_nss_fp8(*args(cols=3070)) == 3
+    assert L.fp8q_nss_fp8(*args(eps=-1.0)) == 7
+    torch.cuda.synchronize()
+
+
+def test_runs_on_a_side_stream_and_is_deterministic():
+    inp = W.config_inputs("nss_qwen", rows=512)
+    x, sc, sh, s = (G.dev_bf16(inp["x"]), G.dev_bf16(inp["scale"]), G.dev_bf16(inp["shift"]),
+                    G.dev_scale(0.25))
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        y1, q1 = fq().nss_fp8(x, sc, sh, s)
+    st.synchronize()
+    y2, q2 = fq().nss_fp8(x, sc, sh, s)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(q1.view(torch.uint8), q2.view(torch.uint8))

@@ -206,14 +206,21 @@ def test_bf16_fma_matches_exact_arithmetic():
     n = 3000
     a, b, c = _random_bf16(rng, n), _random_bf16(rng, n), _random_bf16(rng, n)
     # constructed ties: a*b exactly on a bf16 midpoint, c tiny (+, -, 0)
+    ties = exact.bf16_product_ties()
+    assert len(ties) > 100
     ta, tb, tc = [], [], []
-    for _ in range(600):
-        m1 = int(rng.integers(128, 256)) | 1
-        m2 = 129
+    for i in range(600):
+        m1, m2 = ties[int(rng.integers(len(ties)))]
         e1, e2 = int(rng.integers(-20, 20)), int(rng.integers(-20, 20))
-        ta.append(bf(m1 * 2.0 ** e1))
+        sgn = float(rng.choice([1.0, -1.0]))
+        ta.append(bf(sgn * m1 * 2.0 ** e1))
         tb.append(bf(m2 * 2.0 ** e2))
-        tc.append(bf(float(rng.choice([1.0, -1.0, 0.0])) * 2.0 ** (e1 + e2 - 10)))
+        tc.append(bf(float([1.0, -1.0, 0.0][i % 3]) * 2.0 ** (e1 + e2 - 10)))
+    # the constructed products really are ties
+    for i in range(20):
+        p = F(exact.bf16_value(ta[i])) * F(exact.bf16_value(tb[i]))
+        lo = exact.nearest_bf16(p)
+        assert exact.nearest_bf16(p + p / 2 ** 40) != exact.nearest_bf16(p - p / 2 ** 40)
     a = np.concatenate([a, ta]).astype(np.uint16)
     b = np.concatenate([b, tb]).astype(np.uint16)
     c = np.concatenate([c, tc]).astype(np.uint16)
