@@ -407,6 +407,22 @@ def roofline_entry(case: Case, ms_per_launch: float, peak: float, peak_src: str)
             "kernel": case.name}
 
 
+def max_over_ranks(ms: float, device: str = "cuda") -> float:
+    """Slowest rank's elapsed time (the job finishes when the last replica does)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(rows_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank processes rows_per_step rows per step."""
+    return rows_per_step * steps * world / (max_ms / 1e3)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -440,13 +456,10 @@ def run_ours(args):
                                barrier=barrier)
     finally:
         sampler.stop()
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, "cuda")
     clocks = sampler.summary(t0, t1)
     ms_step = ms / args.steps
-    value = main.rows * args.steps * world / (ms / 1e3)
+    value = job_rows_per_s(main.rows, args.steps, world, ms)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,

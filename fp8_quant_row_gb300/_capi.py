@@ -19,7 +19,8 @@ STATUS = {0: "FP8Q_OK", 1: "FP8Q_ERR_NULL", 2: "FP8Q_ERR_ALIGN", 3: "FP8Q_ERR_SH
 
 #: every function include/fp8q.h declares
 SYMBOLS = ("fp8q_nss_fp8", "fp8q_scale_residual_nss_fp8", "fp8q_bias_mul_add",
-           "fp8q_token_cat_fp8", "fp8q_status_string", "fp8q_last_cuda_error", "fp8q_version")
+           "fp8q_token_cat_fp8", "fp8q_status_string", "fp8q_last_cuda_error",
+           "fp8q_last_error_detail", "fp8q_version")
 
 
 class Fp8qError(RuntimeError):
@@ -27,7 +28,8 @@ class Fp8qError(RuntimeError):
         self.status = int(status)
         msg = lib().fp8q_status_string(self.status).decode()
         if self.status == 6:
-            msg += f" (cudaError_t {lib().fp8q_last_cuda_error()})"
+            msg += (f" (cudaError_t {lib().fp8q_last_cuda_error()}: "
+                    f"{lib().fp8q_last_error_detail().decode()})")
         super().__init__(f"{where}: {STATUS.get(self.status, self.status)}: {msg}")
 
 
@@ -54,6 +56,8 @@ def lib():
         L.fp8q_status_string.restype = ctypes.c_char_p
         L.fp8q_last_cuda_error.argtypes = []
         L.fp8q_last_cuda_error.restype = i32
+        L.fp8q_last_error_detail.argtypes = []
+        L.fp8q_last_error_detail.restype = ctypes.c_char_p
         L.fp8q_version.argtypes = []
         L.fp8q_version.restype = i32
         _lib = L

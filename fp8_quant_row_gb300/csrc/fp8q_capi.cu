@@ -7,6 +7,7 @@
 // attributes).
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -23,6 +24,7 @@ constexpr int64_t kMaxLnCols = 32768;
 constexpr int64_t kMaxEwCols = int64_t(1) << 30;
 
 thread_local int g_last_cuda_error = 0;
+thread_local char g_last_detail[160] = "";
 
 struct DeviceInfo {
   int major = 0, minor = 0, sms = 0, smem_optin = 0;
@@ -32,8 +34,11 @@ struct DeviceInfo {
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_dev_once[kMaxDevices];
 
-fp8q_status cuda_fail(cudaError_t e) {
+// Records which runtime call failed (thread-local) and returns FP8Q_ERR_CUDA.
+fp8q_status cuda_fail(cudaError_t e, const char* site, long long arg = -1) {
   g_last_cuda_error = int(e);
+  std::snprintf(g_last_detail, sizeof g_last_detail, "%s(%lld): %s", site, arg,
+                cudaGetErrorName(e));
   return FP8Q_ERR_CUDA;
 }
 
@@ -41,7 +46,7 @@ fp8q_status cuda_fail(cudaError_t e) {
 fp8q_status current_device(const DeviceInfo** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return FP8Q_ERR_UNSUPPORTED;
   std::call_once(g_dev_once[dev], [dev] {
     DeviceInfo& d = g_dev[dev];
@@ -52,7 +57,7 @@ fp8q_status current_device(const DeviceInfo** out) {
                cudaSuccess;
   });
   const DeviceInfo& d = g_dev[dev];
-  if (!d.ok) return cuda_fail(cudaErrorInvalidDevice);
+  if (!d.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaDeviceGetAttribute", dev);
   if (d.major != 10 || d.minor != 3) return FP8Q_ERR_UNSUPPORTED;
   *out = &d;
   return FP8Q_OK;
@@ -72,7 +77,7 @@ std::mutex g_occ_mu;
 fp8q_status blocks_per_sm(const void* fn, int threads, size_t smem, int* blocks) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   std::lock_guard<std::mutex> lock(g_occ_mu);
   for (int i = 0; i < g_occ_n; ++i)
     if (g_occ[i].dev == dev && g_occ[i].fn == fn && g_occ[i].smem == smem) {
@@ -81,11 +86,11 @@ fp8q_status blocks_per_sm(const void* fn, int threads, size_t smem, int* blocks)
     }
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return cuda_fail(e);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)", (long long)smem);
   }
   int b = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
-  if (e != cudaSuccess) return cuda_fail(e);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor", (long long)smem);
   if (g_occ_n < 256) g_occ[g_occ_n++] = OccEntry{dev, fn, smem, b};
   *blocks = b;
   return FP8Q_OK;
@@ -106,9 +111,16 @@ bool overlap(Range a, Range b) {
 
 bool same(Range a, Range b) { return a.p == b.p && a.bytes == b.bytes; }
 
-fp8q_status launch_status() {
-  const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? FP8Q_OK : cuda_fail(e);
+// One launch; the status is this launch's own (cudaLaunchKernel's return value), so an
+// unrelated pending error of another library on the same thread is never reported as ours.
+template <typename... Args>
+fp8q_status launch(void (*fn)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                   Args... args) {
+  void* argv[] = {static_cast<void*>(&args)...};
+  const cudaError_t e =
+      cudaLaunchKernel(reinterpret_cast<const void*>(fn), grid, block, argv, smem, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel", (long long)smem);
+  return FP8Q_OK;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -120,22 +132,26 @@ fp8q_status launch_tuned(const fp8q::NssParams& p, const DeviceInfo& dev, int64_
                          cudaStream_t stream, bool* launched) {
   using L = fp8q::TunedLayout<V, WPR, RESID>;
   auto* fn = fp8q::nss_tuned_kernel<V, WPR, RESID, HAS_BIAS>;
-  const int slots = n_mod > 1 ? 2 : 1;
-  const size_t smem = L::smem_bytes(slots);
   *launched = false;
-  if (smem > size_t(dev.smem_optin)) return FP8Q_OK;
+  // As many warps per CTA (one CTA per SM) as the shared-memory ring allows, up to 16.
+  int nw = fp8q::kTunedMaxThreads / 32;
+  while (nw >= WPR && L::smem_bytes(nw) > size_t(dev.smem_optin)) nw -= WPR;
+  nw -= nw % WPR;
+  if (nw < WPR) return FP8Q_OK;
+  const size_t smem = L::smem_bytes(nw);
   int bps = 0;
-  fp8q_status st = blocks_per_sm(reinterpret_cast<const void*>(fn), fp8q::kNssThreads, smem, &bps);
+  fp8q_status st = blocks_per_sm(reinterpret_cast<const void*>(fn), nw * 32, smem, &bps);
   if (st != FP8Q_OK) return st;
   if (bps <= 0) return FP8Q_OK;
-  const int64_t need = (p.rows + L::kRowsPerIter - 1) / L::kRowsPerIter;
-  int64_t grid = int64_t(dev.sms) * bps;
-  if (grid > need) grid = need;
-  // A CTA's contiguous row block may touch at most two modulation rows.
-  if (p.mod_rows > 0 && n_mod > 1 && p.mod_rows < (p.rows + grid - 1) / grid) return FP8Q_OK;
-  fn<<<dim3(unsigned(grid)), dim3(fp8q::kNssThreads), smem, stream>>>(p);
+  const int rows_per_iter = nw / WPR;
+  const int64_t need = (p.rows + rows_per_iter - 1) / rows_per_iter;
+  const int64_t cap = int64_t(dev.sms) * bps;
+  int64_t grid = need > n_mod ? need : n_mod;
+  if (grid > cap) grid = cap;
+  // Every CTA must sit inside one modulation group (single-row table).
+  if (n_mod > grid) return FP8Q_OK;
   *launched = true;
-  return launch_status();
+  return launch(fn, dim3(unsigned(grid)), dim3(nw * 32), smem, stream, p, n_mod);
 }
 
 template <bool RESID, bool HAS_BIAS>
@@ -145,11 +161,10 @@ fp8q_status launch_generic(const fp8q::NssParams& p, const DeviceInfo& dev, cuda
   int bps = 0;
   fp8q_status st = blocks_per_sm(reinterpret_cast<const void*>(fn), fp8q::kNssThreads, smem, &bps);
   if (st != FP8Q_OK) return st;
-  if (bps <= 0) return cuda_fail(cudaErrorInvalidConfiguration);
+  if (bps <= 0) return cuda_fail(cudaErrorInvalidConfiguration, "occupancy", (long long)smem);
   int64_t grid = int64_t(dev.sms) * bps;
   if (grid > p.rows) grid = p.rows;
-  fn<<<dim3(unsigned(grid)), dim3(fp8q::kNssThreads), smem, stream>>>(p);
-  return launch_status();
+  return launch(fn, dim3(unsigned(grid)), dim3(fp8q::kNssThreads), smem, stream, p);
 }
 
 template <bool RESID, bool HAS_BIAS>
@@ -292,11 +307,10 @@ fp8q_status fp8q_bias_mul_add(void* y_bf16, const void* x_bf16, const void* bias
   const unsigned gy = unsigned((chunks + per_cta - 1) / per_cta);
   const unsigned gx = unsigned(rows < 0x7FFFFFFF ? rows : 0x7FFFFFFF);
   if (gy > 65535u) return FP8Q_ERR_SHAPE;
-  fp8q::bias_mul_add_kernel<<<dim3(gx, gy), dim3(fp8q::kEwThreads), 0, stream>>>(
-      static_cast<uint16_t*>(y_bf16), static_cast<const uint16_t*>(x_bf16),
-      static_cast<const uint16_t*>(bias_bf16), static_cast<const uint16_t*>(gate_bf16),
-      static_cast<const uint16_t*>(residual_bf16), rows, int(cols));
-  return launch_status();
+  return launch(fp8q::bias_mul_add_kernel, dim3(gx, gy), dim3(fp8q::kEwThreads), 0, stream,
+                static_cast<uint16_t*>(y_bf16), static_cast<const uint16_t*>(x_bf16),
+                static_cast<const uint16_t*>(bias_bf16), static_cast<const uint16_t*>(gate_bf16),
+                static_cast<const uint16_t*>(residual_bf16), rows, int(cols));
 }
 
 fp8q_status fp8q_token_cat_fp8(uint8_t* q_e4m3, const void* a_bf16, int64_t a_cols,
@@ -321,10 +335,9 @@ fp8q_status fp8q_token_cat_fp8(uint8_t* q_e4m3, const void* a_bf16, int64_t a_co
   const unsigned gy = unsigned((chunks + per_cta - 1) / per_cta);
   const unsigned gx = unsigned(rows < 0x7FFFFFFF ? rows : 0x7FFFFFFF);
   if (gy > 65535u) return FP8Q_ERR_SHAPE;
-  fp8q::token_cat_fp8_kernel<<<dim3(gx, gy), dim3(fp8q::kEwThreads), 0, stream>>>(
-      q_e4m3, static_cast<const uint16_t*>(a_bf16), int(a_cols),
-      static_cast<const uint16_t*>(m_bf16), int(m_cols), input_scale, rows);
-  return launch_status();
+  return launch(fp8q::token_cat_fp8_kernel, dim3(gx, gy), dim3(fp8q::kEwThreads), 0, stream,
+                q_e4m3, static_cast<const uint16_t*>(a_bf16), int(a_cols),
+                static_cast<const uint16_t*>(m_bf16), int(m_cols), input_scale, rows);
 }
 
 const char* fp8q_status_string(int status) {
@@ -342,6 +355,8 @@ const char* fp8q_status_string(int status) {
 }
 
 int fp8q_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* fp8q_last_error_detail(void) { return g_last_detail; }
 
 int fp8q_version(void) { return 0x000100; }
 

@@ -218,3 +218,70 @@ __device__ __forceinline__ uint32_t quant2(uint32_t ypair, float inv) {
 }
 
 }  // namespace fp8q
+
+namespace fp8q {
+
+// ------------------------------------------------------------------------------------------
+// packed fp32 pairs (sm_100+ f32x2 instructions: one issue slot for two lanes of work)
+// ------------------------------------------------------------------------------------------
+
+struct f2 {
+  unsigned long long v;
+};
+
+__device__ __forceinline__ f2 f2_make(float lo, float hi) {
+  return f2{(static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo)};
+}
+__device__ __forceinline__ float f2_lo(f2 a) { return __uint_as_float(uint32_t(a.v)); }
+__device__ __forceinline__ float f2_hi(f2 a) { return __uint_as_float(uint32_t(a.v >> 32)); }
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  f2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+  f2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return r;
+}
+
+// bf16x2 word -> (lo, hi) fp32 pair.
+__device__ __forceinline__ f2 bf2_to_f2(uint32_t u) { return f2_make(bf_lo(u), bf_hi(u)); }
+
+// Knuth TwoSum on both lanes: s + e == a + b exactly.
+__device__ __forceinline__ void two_sum2(f2 a, f2 b, f2& s, f2& e) {
+  s = add2(a, b);
+  const f2 bv = sub2(s, a);
+  const f2 av = sub2(s, bv);
+  e = add2(sub2(a, av), sub2(b, bv));
+}
+
+// ------------------------------------------------------------------------------------------
+// asynchronous global -> shared copies (cp.async, completion by wait_group: no spin loops)
+// ------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+}  // namespace fp8q

@@ -12,12 +12,14 @@
 // holds V 16-byte chunks of it in registers (chunk j of lane l covers columns
 // [(j*32 + l)*8, +8) of the warp's part), so every global load and store of a warp is one
 // contiguous 512-byte (bf16) or 256-byte (e4m3) segment. The row sums sum(x) and sum(x^2)
-// are accumulated error-free (TwoSum) per lane and reduced across the warp by an xor
-// butterfly of double-float additions (commutative, so every lane ends with bit-identical
-// row constants). RN(1 + scale) and shift are pre-expanded once per CTA into shared memory
-// as fp32 in lane-major order, so each warp-wide 16-byte shared load is conflict-free. CTAs
-// are persistent and own a contiguous block of rows; a block touches at most two modulation
-// rows, which is why the table has at most two slots.
+// are accumulated error-free (TwoSum, on packed fp32 pairs) per lane and reduced across the
+// warp by an xor butterfly of double-float additions (commutative, so every lane ends with
+// bit-identical row constants). Each warp streams its rows through a two-stage cp.async ring
+// in shared memory, so the next row is in flight while the current one is processed.
+// RN(1 + scale) and shift are expanded once per CTA into shared memory as fp32 in lane-major
+// order (each warp-wide 16-byte shared load is conflict-free). CTAs are persistent, own a
+// contiguous block of rows, and with per-sample modulation are assigned to one modulation
+// group each, so the table holds a single modulation row.
 //
 // Generic path (any cols % 8 == 0 up to 32768): one CTA per row, the row staged in shared
 // memory, same per-element arithmetic.
@@ -132,119 +134,195 @@ __device__ __forceinline__ void modulate_quant8(const uint4& n, const float* ops
 // tuned path
 // ------------------------------------------------------------------------------------------
 
-// Shared-memory table layout (float4 units), per modulation slot s, row part w, chunk j,
-// piece k, lane l: index (((s*WPR + w)*V + j)*P + k)*32 + l. Pieces: 0,1 = RN(1+scale) for
-// the chunk's 8 columns, 2,3 = shift; residual variant adds 4 = gate (8 bf16), 5 = bias.
+constexpr int kTunedMaxThreads = 512;
+constexpr int kStages = 2;
+
+// Shared memory of the tuned kernel: [table | ring | exchange].
+//   table    float4 index (((w*V + j)*P + k)*32 + l) for row part w, chunk j, piece k, lane l.
+//            Pieces: 0,1 = RN(1+scale) of the chunk's 8 columns, 2,3 = shift; the residual
+//            variant adds 4 = gate (8 bf16) and 5 = bias (8 bf16).
+//   ring     per warp, kStages row buffers (x, and residual for the residual variant), filled
+//            by cp.async one row ahead of the row being processed.
+//   exchange (two warps per row) double-buffered partial sums, one float4 per warp.
 template <int V, int WPR, bool RESID>
 struct TunedLayout {
   static constexpr int kCols = 256 * V * WPR;
+  static constexpr int kPartCols = kCols / WPR;
   static constexpr int kPieces = RESID ? 6 : 4;
-  static constexpr int kSlotF4 = WPR * V * kPieces * 32;       // float4 per slot
-  static constexpr int kRowsPerIter = kNssWarps / WPR;
-  static constexpr int kRedF4 = 2 * kRowsPerIter * WPR;         // WPR>1 exchange buffers
-  static constexpr size_t smem_bytes(int slots) {
-    return (size_t(slots) * kSlotF4 + (WPR > 1 ? kRedF4 : 0)) * sizeof(float4);
+  static constexpr int kTableF4 = WPR * V * kPieces * 32;
+  static constexpr int kStageBytes = kPartCols * 2 * (RESID ? 2 : 1);
+  static constexpr size_t smem_bytes(int nw) {
+    return size_t(kTableF4) * 16 + size_t(nw) * kStages * kStageBytes +
+           (WPR > 1 ? size_t(2 * nw) * 16 : 0);
   }
 };
 
+// Rows of CTA b out of G. Without per-sample modulation the rows are split evenly. With
+// n_mod modulation groups (n_mod <= G) the CTAs are first divided among the groups, so every
+// CTA works inside one group and needs a single modulation row.
+struct RowBlock {
+  int64_t begin, end, mod;
+};
+
+__device__ __forceinline__ RowBlock cta_rows(int64_t rows, int64_t mod_rows, int64_t n_mod,
+                                             int64_t b, int64_t G) {
+  if (n_mod <= 1) return RowBlock{rows * b / G, rows * (b + 1) / G, 0};
+  const int64_t g = b * n_mod / G;
+  const int64_t c0 = (g * G + n_mod - 1) / n_mod;        // first CTA of group g
+  const int64_t c1 = ((g + 1) * G + n_mod - 1) / n_mod;  // first CTA of group g + 1
+  const int64_t k = c1 - c0, i = b - c0;
+  const int64_t g0 = g * mod_rows;
+  const int64_t rg = rows - g0 < mod_rows ? rows - g0 : mod_rows;
+  return RowBlock{g0 + rg * i / k, g0 + rg * (i + 1) / k, g};
+}
+
+__device__ __forceinline__ dd dd_norm(float hi, float lo) {
+  dd r;
+  two_sum(hi, lo, r.hi, r.lo);
+  return r;
+}
+
+// Exact-path fix-up of one 8-element chunk (rare: called only when some element of the chunk
+// is uncertain). Out of line so that the hot loop stays small.
+__device__ __noinline__ uint4 fix_uncertain8(const uint4 x, const uint4 n, const RowConst kc) {
+  const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+  uint32_t nw[4] = {n.x, n.y, n.z, n.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t lo = nw[i] & 0xFFFFu, hi = nw[i] >> 16;
+    if (norm_uncertain(norm_fast(bf_lo(xw[i]), kc), kc)) lo = norm_exact_bits(bf_lo(xw[i]), kc);
+    if (norm_uncertain(norm_fast(bf_hi(xw[i]), kc), kc)) hi = norm_exact_bits(bf_hi(xw[i]), kc);
+    nw[i] = lo | (hi << 16);
+  }
+  return make_uint4(nw[0], nw[1], nw[2], nw[3]);
+}
+
 template <int V, int WPR, bool RESID, bool HAS_BIAS>
-__global__ void __launch_bounds__(kNssThreads, 1) nss_tuned_kernel(const NssParams p) {
+__global__ void __launch_bounds__(kTunedMaxThreads, 1)
+    nss_tuned_kernel(const NssParams p, const int64_t n_mod) {
   using L = TunedLayout<V, WPR, RESID>;
   constexpr int C = L::kCols;
+  constexpr int PC = L::kPartCols;
   constexpr int P = L::kPieces;
-  extern __shared__ float4 smem[];
-  float4* table = smem;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float4* table = reinterpret_cast<float4*>(smem_raw);
+  const int nw = blockDim.x >> 5;
+  const int rows_per_iter = nw / WPR;
+  unsigned char* ring = smem_raw + size_t(L::kTableF4) * 16;
+  float4* red = reinterpret_cast<float4*>(ring + size_t(nw) * kStages * L::kStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row_slot = warp / WPR, part = warp % WPR;
-  const int64_t rb = (p.rows * blockIdx.x) / gridDim.x;
-  const int64_t re = (p.rows * (blockIdx.x + 1)) / gridDim.x;
-  if (rb >= re) return;  // uniform across the CTA
-  const int64_t m_lo = p.mod_rows > 0 ? rb / p.mod_rows : 0;
-  const int64_t m_hi = p.mod_rows > 0 ? (re - 1) / p.mod_rows : 0;
-  const int slots = int(m_hi - m_lo + 1);  // host guarantees <= 2
+  const RowBlock blk = cta_rows(p.rows, p.mod_rows, n_mod, blockIdx.x, gridDim.x);
+  if (blk.begin >= blk.end) return;  // uniform across the CTA
+  unsigned char* my_ring = ring + size_t(warp) * kStages * L::kStageBytes;
 
-  // Build the modulation table: one float4 per (slot, part, chunk, piece, lane).
-  for (int idx = threadIdx.x; idx < slots * L::kSlotF4; idx += kNssThreads) {
-    const int l = idx & 31;
-    int rest = idx >> 5;
-    const int k = rest % P;
-    rest /= P;
-    const int j = rest % V;
-    rest /= V;
-    const int w = rest % WPR;
-    const int s = rest / WPR;
-    const int col = w * (C / WPR) + (j * 32 + l) * 8;
-    const int64_t mrow = (m_lo + s) * C;
-    float4 out;
-    if (k < 4) {
-      const uint16_t* src = (k < 2 ? p.scale : p.shift) + mrow + col + (k & 1) * 4;
-      const uint2 raw = *reinterpret_cast<const uint2*>(src);
-      float a = bf_lo(raw.x), b = bf_hi(raw.x), c = bf_lo(raw.y), d = bf_hi(raw.y);
-      if (k < 2) {
-        a = __fadd_rn(1.0f, a);
-        b = __fadd_rn(1.0f, b);
-        c = __fadd_rn(1.0f, c);
-        d = __fadd_rn(1.0f, d);
-      }
-      out = make_float4(a, b, c, d);
-    } else {
-      uint4 raw = make_uint4(0, 0, 0, 0);
-      if (k == 4) raw = *reinterpret_cast<const uint4*>(p.gate + mrow + col);
-      else if (HAS_BIAS) raw = *reinterpret_cast<const uint4*>(p.bias + col);
-      out = make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y), __uint_as_float(raw.z),
-                        __uint_as_float(raw.w));
+  // Row r's part for this warp -> ring stage (each lane copies exactly the chunks it reads).
+  auto issue = [&](int64_t r, int stage) {
+    const size_t off = size_t(r) * C + size_t(part) * PC;
+    uint4* dst = reinterpret_cast<uint4*>(my_ring + stage * L::kStageBytes) + lane;
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + off) + lane;
+#pragma unroll
+    for (int j = 0; j < V; ++j) cp_async16(dst + j * 32, src + j * 32);
+    if constexpr (RESID) {
+      const uint4* src2 = reinterpret_cast<const uint4*>(p.residual + off) + lane;
+#pragma unroll
+      for (int j = 0; j < V; ++j) cp_async16(dst + (PC / 8) + j * 32, src2 + j * 32);
     }
-    table[idx] = out;
+  };
+
+  int64_t r = blk.begin + row_slot;
+  if (r < blk.end) issue(r, 0);
+  cp_async_commit();
+
+  // Modulation table of this CTA's group, built while the first rows are in flight.
+  {
+    const size_t mrow = size_t(blk.mod) * C;
+    constexpr int kUnits = WPR * V * 32;
+#pragma unroll 1
+    for (int u = threadIdx.x; u < kUnits; u += blockDim.x) {
+      const int l = u & 31, jw = u >> 5;  // jw = w*V + j
+      const size_t col = size_t(jw / V) * PC + size_t((jw % V) * 32 + l) * 8;
+      const uint4 sc = __ldg(reinterpret_cast<const uint4*>(p.scale + mrow + col));
+      const uint4 sh = __ldg(reinterpret_cast<const uint4*>(p.shift + mrow + col));
+      uint4 g = make_uint4(0, 0, 0, 0), b = g;
+      if constexpr (RESID) {
+        g = __ldg(reinterpret_cast<const uint4*>(p.gate + mrow + col));
+        if (HAS_BIAS) b = __ldg(reinterpret_cast<const uint4*>(p.bias + col));
+      }
+      float4* t = table + size_t(jw) * P * 32 + l;
+      t[0 * 32] = make_float4(__fadd_rn(1.0f, bf_lo(sc.x)), __fadd_rn(1.0f, bf_hi(sc.x)),
+                              __fadd_rn(1.0f, bf_lo(sc.y)), __fadd_rn(1.0f, bf_hi(sc.y)));
+      t[1 * 32] = make_float4(__fadd_rn(1.0f, bf_lo(sc.z)), __fadd_rn(1.0f, bf_hi(sc.z)),
+                              __fadd_rn(1.0f, bf_lo(sc.w)), __fadd_rn(1.0f, bf_hi(sc.w)));
+      t[2 * 32] = make_float4(bf_lo(sh.x), bf_hi(sh.x), bf_lo(sh.y), bf_hi(sh.y));
+      t[3 * 32] = make_float4(bf_lo(sh.z), bf_hi(sh.z), bf_lo(sh.w), bf_hi(sh.w));
+      if constexpr (RESID) {
+        t[4 * 32] = make_float4(__uint_as_float(g.x), __uint_as_float(g.y), __uint_as_float(g.z),
+                                __uint_as_float(g.w));
+        t[5 * 32] = make_float4(__uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z),
+                                __uint_as_float(b.w));
+      }
+    }
   }
   __syncthreads();
 
   const float inv = __frcp_rn(__ldg(p.input_scale));
+  const f2 inv2 = f2_make(inv, inv);
   const float colsf = float(C);
-  float4* red = smem + size_t(slots) * L::kSlotF4;  // WPR > 1 exchange, double-buffered
+  const float4* tab = table + size_t(part) * V * P * 32 + lane;
   int parity = 0;
 
-  for (int64_t r = rb + row_slot; r < re; r += L::kRowsPerIter) {
-    const int s = p.mod_rows > 0 ? int(r / p.mod_rows - m_lo) : 0;
-    const float4* tab = table + size_t(s * WPR + part) * V * P * 32 + lane;
-    const size_t row_off = size_t(r) * C + size_t(part) * (C / WPR);
+#pragma unroll 1
+  for (int k = 0; r < blk.end; ++k, r += rows_per_iter) {
+    const int64_t rn = r + rows_per_iter;
+    if (rn < blk.end) issue(rn, (k + 1) & 1);
+    cp_async_commit();
+    cp_async_wait<1>();  // this lane's copies of row r have landed
+    const size_t row_off = size_t(r) * C + size_t(part) * PC;
+    uint4* stage = reinterpret_cast<uint4*>(my_ring + (k & 1) * L::kStageBytes) + lane;
 
-    uint4 xv[V];
-    {
-      const uint4* xr = reinterpret_cast<const uint4*>(p.x + row_off) + lane;
-#pragma unroll
-      for (int j = 0; j < V; ++j) xv[j] = ld_stream(xr + j * 32);
-    }
     if constexpr (RESID) {
-      const uint4* rr = reinterpret_cast<const uint4*>(p.residual + row_off) + lane;
+      // residual_out replaces x in the stage; each lane rewrites only its own chunks.
       uint4* ro = reinterpret_cast<uint4*>(p.residual_out + row_off) + lane;
-      uint4 rv[V];
-#pragma unroll
-      for (int j = 0; j < V; ++j) rv[j] = ld_stream(rr + j * 32);
-#pragma unroll
+#pragma unroll 2
       for (int j = 0; j < V; ++j) {
+        const uint4 xv = stage[j * 32], rv = stage[(PC / 8) + j * 32];
         const float4 gf = tab[(j * P + 4) * 32];
         const float4 bf = tab[(j * P + 5) * 32];
-        const uint32_t g[4] = {__float_as_uint(gf.x), __float_as_uint(gf.y),
-                               __float_as_uint(gf.z), __float_as_uint(gf.w)};
-        const uint32_t b[4] = {__float_as_uint(bf.x), __float_as_uint(bf.y),
-                               __float_as_uint(bf.z), __float_as_uint(bf.w)};
         uint4 o;
-        o.x = resid2<HAS_BIAS>(xv[j].x, b[0], g[0], rv[j].x);
-        o.y = resid2<HAS_BIAS>(xv[j].y, b[1], g[1], rv[j].y);
-        o.z = resid2<HAS_BIAS>(xv[j].z, b[2], g[2], rv[j].z);
-        o.w = resid2<HAS_BIAS>(xv[j].w, b[3], g[3], rv[j].w);
-        xv[j] = o;
+        o.x = resid2<HAS_BIAS>(xv.x, __float_as_uint(bf.x), __float_as_uint(gf.x), rv.x);
+        o.y = resid2<HAS_BIAS>(xv.y, __float_as_uint(bf.y), __float_as_uint(gf.y), rv.y);
+        o.z = resid2<HAS_BIAS>(xv.z, __float_as_uint(bf.z), __float_as_uint(gf.z), rv.z);
+        o.w = resid2<HAS_BIAS>(xv.w, __float_as_uint(bf.w), __float_as_uint(gf.w), rv.w);
+        stage[j * 32] = o;
         st_stream(ro + j * 32, o);
       }
     }
 
-    dd s1{0.0f, 0.0f}, s2{0.0f, 0.0f};
+    // Row sums, error-free per element (TwoSum on both halves of each bf16 pair).
+    f2 sx = f2_make(0.0f, 0.0f), ex = sx, sq = sx, eq = sx;
+#pragma unroll 2
+    for (int j = 0; j < V; ++j) {
+      const uint4 xv = stage[j * 32];
+      const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-    for (int j = 0; j < V; ++j) acc_stats8(xv[j], s1, s2);
+      for (int i = 0; i < 4; ++i) {
+        const f2 v = bf2_to_f2(w4[i]);
+        f2 s, e;
+        two_sum2(sx, v, s, e);
+        sx = s;
+        ex = add2(ex, e);
+        two_sum2(sq, mul2(v, v), s, e);  // v*v exact: 8-bit significands
+        sq = s;
+        eq = add2(eq, e);
+      }
+    }
+    dd s1 = dd_add(dd_norm(f2_lo(sx), f2_lo(ex)), dd_norm(f2_hi(sx), f2_hi(ex)));
+    dd s2 = dd_add(dd_norm(f2_lo(sq), f2_lo(eq)), dd_norm(f2_hi(sq), f2_hi(eq)));
     warp_reduce_dd(s1, s2);
     if constexpr (WPR > 1) {
-      float4* buf = red + parity * (L::kRowsPerIter * WPR) + row_slot * WPR;
+      float4* buf = red + parity * nw + row_slot * WPR;
       if (lane == 0) buf[part] = make_float4(s1.hi, s1.lo, s2.hi, s2.lo);
       asm volatile("bar.sync %0, %1;" ::"r"(1 + row_slot), "r"(32 * WPR) : "memory");
       const float4 a0 = buf[0];
@@ -258,26 +336,47 @@ __global__ void __launch_bounds__(kNssThreads, 1) nss_tuned_kernel(const NssPara
       }
       parity ^= 1;
     }
-    const RowConst k = row_constants(s1, s2, colsf, p.eps);
+    const RowConst kc = row_constants(s1, s2, colsf, p.eps);
+    const f2 mu2 = f2_make(kc.mu_hi, kc.mu_hi), r2 = f2_make(kc.r_hi, kc.r_hi),
+             c2 = f2_make(kc.c, kc.c);
 
     uint4* yr = reinterpret_cast<uint4*>(p.y + row_off) + lane;
     uint2* qr = reinterpret_cast<uint2*>(p.q + row_off) + lane;
-#pragma unroll
+#pragma unroll 1
     for (int j = 0; j < V; ++j) {
-      const uint4 n = normalise8(xv[j], k);
-      const float4 o0 = tab[(j * P + 0) * 32];
-      const float4 o1 = tab[(j * P + 1) * 32];
-      const float4 h0 = tab[(j * P + 2) * 32];
-      const float4 h1 = tab[(j * P + 3) * 32];
-      const float ops[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-      const float sh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-      uint4 y;
-      uint2 q;
-      modulate_quant8(n, ops, sh, inv, y, q);
-      st_stream(yr + j * 32, y);
-      st_stream(qr + j * 32, q);
+      const uint4 xv = stage[j * 32];
+      const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
+      uint32_t n[4];
+      bool any = false;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const f2 tt = fma2(sub2(bf2_to_f2(w4[i]), mu2), r2, c2);
+        const float t0 = f2_lo(tt), t1 = f2_hi(tt);
+        any |= norm_uncertain(t0, kc) | norm_uncertain(t1, kc);
+        n[i] = pack_bf16x2(t0, t1);
+      }
+      uint4 nv = make_uint4(n[0], n[1], n[2], n[3]);
+      if (any) nv = fix_uncertain8(xv, nv, kc);
+      const float4 o0 = tab[(j * P + 0) * 32], o1 = tab[(j * P + 1) * 32];
+      const float4 h0 = tab[(j * P + 2) * 32], h1 = tab[(j * P + 3) * 32];
+      const uint32_t nn[4] = {nv.x, nv.y, nv.z, nv.w};
+      const f2 ops[4] = {f2_make(o0.x, o0.y), f2_make(o0.z, o0.w), f2_make(o1.x, o1.y),
+                         f2_make(o1.z, o1.w)};
+      const f2 shs[4] = {f2_make(h0.x, h0.y), f2_make(h0.z, h0.w), f2_make(h1.x, h1.y),
+                         f2_make(h1.z, h1.w)};
+      uint32_t yw[4], qw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const f2 yf = fma2(bf2_to_f2(nn[i]), ops[i], shs[i]);
+        yw[i] = pack_bf16x2(f2_lo(yf), f2_hi(yf));
+        const f2 qf = mul2(bf2_to_f2(yw[i]), inv2);
+        qw[i] = pack_e4m3x2(f2_lo(qf), f2_hi(qf));
+      }
+      st_stream(yr + j * 32, make_uint4(yw[0], yw[1], yw[2], yw[3]));
+      st_stream(qr + j * 32, make_uint2(qw[0] | (qw[1] << 16), qw[2] | (qw[3] << 16)));
     }
   }
+  cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------------------------------

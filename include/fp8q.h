@@ -142,6 +142,10 @@ const char* fp8q_status_string(int status);
 /* cudaError_t of the last FP8Q_ERR_CUDA returned on the calling host thread (0 if none). */
 int fp8q_last_cuda_error(void);
 
+/* Which runtime call produced that error, e.g. "cudaLaunchKernel(98560): cudaErrorInvalidValue"
+ * (thread-local static string, "" if none; overwritten by the next failure). */
+const char* fp8q_last_error_detail(void);
+
 /* Library ABI version: 0x00MMmmpp. */
 int fp8q_version(void);
 
