@@ -544,6 +544,24 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_only(args):
+    """Launch one workload W + K times with no timing and no JSON (for ncu captures)."""
+    import torch
+    import fp8_quant_row_gb300 as fq
+    torch.cuda.set_device(0)
+    fq.build()
+    lib = fq._capi.lib()
+    l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20))
+    if args.profile_only == "nss_qwen":
+        case = make_cases(torch, fq, lib, l2)["nss_qwen"]
+    else:
+        case = extra_cases(torch, lib, l2)[args.profile_only]
+    for i in range(args.warmup + args.steps):
+        case.launch(i)
+    torch.cuda.synchronize()
+    log(f"profile-only {args.profile_only}: {args.warmup + args.steps} launches of {case.name}")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -555,10 +573,15 @@ def main():
     ap.add_argument("--skip-kernels", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile-only", choices=("nss_qwen", "scale_residual_qwen",
+                                               "bias_mul_add_qwen", "nss_flux", "token_cat_flux"),
+                    help="only launch this workload (W+K launches, no timing): for ncu captures")
     args = ap.parse_args()
-    if args.warmup < 3:
+    if args.warmup < 3 and not args.profile_only:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.profile_only:
+        run_profile_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -20,6 +20,8 @@ constexpr int kEwThreads = 128;
 constexpr int kBmaUnroll = 3;  // 128 threads x 3 chunks x 8 = 3072 columns per CTA
 constexpr int kCatUnroll = 8;  // 128 threads x 8 chunks x 8 = 8192 columns per CTA
 
+// RPC rows per CTA step, all of their loads issued before any use.
+template <int RPC>
 __global__ void __launch_bounds__(kEwThreads) bias_mul_add_kernel(
     uint16_t* __restrict__ y, const uint16_t* __restrict__ x, const uint16_t* __restrict__ bias,
     const uint16_t* __restrict__ gate, const uint16_t* __restrict__ residual, int64_t rows,
@@ -28,29 +30,37 @@ __global__ void __launch_bounds__(kEwThreads) bias_mul_add_kernel(
   const int c0 = (blockIdx.y * kEwThreads) * kBmaUnroll + threadIdx.x;
   const uint4* b4 = reinterpret_cast<const uint4*>(bias);
   const uint4* g4 = reinterpret_cast<const uint4*>(gate);
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const uint4* x4 = reinterpret_cast<const uint4*>(x + size_t(r) * cols);
-    const uint4* r4 = reinterpret_cast<const uint4*>(residual + size_t(r) * cols);
-    uint4* y4 = reinterpret_cast<uint4*>(y + size_t(r) * cols);
-    uint4 xv[kBmaUnroll], rv[kBmaUnroll];
+  wait_for_producers();
+  for (int64_t r0 = int64_t(blockIdx.x) * RPC; r0 < rows; r0 += int64_t(gridDim.x) * RPC) {
+    uint4 xv[RPC][kBmaUnroll], rv[RPC][kBmaUnroll];
 #pragma unroll
-    for (int u = 0; u < kBmaUnroll; ++u) {
-      const int c = c0 + u * kEwThreads;
-      if (c < chunks) {
-        xv[u] = ld_stream(x4 + c);
-        rv[u] = ld_stream(r4 + c);
+    for (int h = 0; h < RPC; ++h) {
+      const int64_t r = r0 + h;
+      const uint4* x4 = reinterpret_cast<const uint4*>(x + size_t(r) * cols);
+      const uint4* r4 = reinterpret_cast<const uint4*>(residual + size_t(r) * cols);
+#pragma unroll
+      for (int u = 0; u < kBmaUnroll; ++u) {
+        const int c = c0 + u * kEwThreads;
+        if (r < rows && c < chunks) {
+          xv[h][u] = ld_stream(x4 + c);
+          rv[h][u] = ld_stream(r4 + c);
+        }
       }
     }
 #pragma unroll
     for (int u = 0; u < kBmaUnroll; ++u) {
       const int c = c0 + u * kEwThreads;
-      if (c < chunks) {
-        const uint4 b = __ldg(b4 + c);
-        const uint4 g = __ldg(g4 + c);
-        const uint32_t xs[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-        const uint32_t bs[4] = {b.x, b.y, b.z, b.w};
-        const uint32_t gs[4] = {g.x, g.y, g.z, g.w};
-        const uint32_t rs[4] = {rv[u].x, rv[u].y, rv[u].z, rv[u].w};
+      if (c >= chunks) continue;
+      const uint4 b = __ldg(b4 + c);
+      const uint4 g = __ldg(g4 + c);
+      const uint32_t bs[4] = {b.x, b.y, b.z, b.w};
+      const uint32_t gs[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int h = 0; h < RPC; ++h) {
+        const int64_t r = r0 + h;
+        if (r >= rows) continue;
+        const uint32_t xs[4] = {xv[h][u].x, xv[h][u].y, xv[h][u].z, xv[h][u].w};
+        const uint32_t rs[4] = {rv[h][u].x, rv[h][u].y, rv[h][u].z, rv[h][u].w};
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -58,7 +68,8 @@ __global__ void __launch_bounds__(kEwThreads) bias_mul_add_kernel(
                                           __fadd_rn(bf_hi(xs[i]), bf_hi(bs[i])));
           o[i] = fma_bf16x2(xb, gs[i], rs[i]);
         }
-        st_stream(y4 + c, make_uint4(o[0], o[1], o[2], o[3]));
+        st_stream(reinterpret_cast<uint4*>(y + size_t(r) * cols) + c,
+                  make_uint4(o[0], o[1], o[2], o[3]));
       }
     }
   }
@@ -78,6 +89,7 @@ __global__ void __launch_bounds__(kEwThreads) token_cat_fp8_kernel(
     uint8_t* __restrict__ q, const uint16_t* __restrict__ a, int a_cols,
     const uint16_t* __restrict__ m, int m_cols, const float* __restrict__ input_scale,
     int64_t rows) {
+  wait_for_producers();
   const float inv = __frcp_rn(__ldg(input_scale));
   const int a_chunks = a_cols / 8;
   const int chunks = (a_cols + m_cols) / 8;

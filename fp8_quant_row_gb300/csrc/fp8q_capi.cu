@@ -111,15 +111,26 @@ bool overlap(Range a, Range b) {
 
 bool same(Range a, Range b) { return a.p == b.p && a.bytes == b.bytes; }
 
-// One launch; the status is this launch's own (cudaLaunchKernel's return value), so an
+// One launch; the status is this launch's own (cudaLaunchKernelEx's return value), so an
 // unrelated pending error of another library on the same thread is never reported as ours.
+// Launches allow programmatic dependent launch: a kernel may be scheduled while the previous
+// kernel in the stream drains, and every kernel executes griddepcontrol.wait before its first
+// global-memory access, so producer -> consumer ordering is unchanged.
 template <typename... Args>
 fp8q_status launch(void (*fn)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                    Args... args) {
-  void* argv[] = {static_cast<void*>(&args)...};
-  const cudaError_t e =
-      cudaLaunchKernel(reinterpret_cast<const void*>(fn), grid, block, argv, smem, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel", (long long)smem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, args...);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx", (long long)smem);
   return FP8Q_OK;
 }
 
@@ -305,12 +316,27 @@ fp8q_status fp8q_bias_mul_add(void* y_bf16, const void* x_bf16, const void* bias
   const int chunks = int(cols / 8);
   const int per_cta = fp8q::kEwThreads * fp8q::kBmaUnroll;
   const unsigned gy = unsigned((chunks + per_cta - 1) / per_cta);
-  const unsigned gx = unsigned(rows < 0x7FFFFFFF ? rows : 0x7FFFFFFF);
   if (gy > 65535u) return FP8Q_ERR_SHAPE;
-  return launch(fp8q::bias_mul_add_kernel, dim3(gx, gy), dim3(fp8q::kEwThreads), 0, stream,
-                static_cast<uint16_t*>(y_bf16), static_cast<const uint16_t*>(x_bf16),
-                static_cast<const uint16_t*>(bias_bf16), static_cast<const uint16_t*>(gate_bf16),
-                static_cast<const uint16_t*>(residual_bf16), rows, int(cols));
+  // Two rows per CTA once one row per CTA would need more than one wave of resident CTAs.
+  auto* fn1 = fp8q::bias_mul_add_kernel<1>;
+  auto* fn2 = fp8q::bias_mul_add_kernel<2>;
+  int bps = 0;
+  st = blocks_per_sm(reinterpret_cast<const void*>(fn2), fp8q::kEwThreads, 0, &bps);
+  if (st != FP8Q_OK) return st;
+  const int64_t wave = int64_t(dev->sms) * (bps > 0 ? bps : 1);
+  const bool two = rows * int64_t(gy) > wave;
+  const int64_t gx64 = two ? (rows + 1) / 2 : rows;
+  const unsigned gx = unsigned(gx64 < 0x7FFFFFFF ? gx64 : 0x7FFFFFFF);
+  auto* yp = static_cast<uint16_t*>(y_bf16);
+  auto* xp = static_cast<const uint16_t*>(x_bf16);
+  auto* bp = static_cast<const uint16_t*>(bias_bf16);
+  auto* gp = static_cast<const uint16_t*>(gate_bf16);
+  auto* rp = static_cast<const uint16_t*>(residual_bf16);
+  if (two)
+    return launch(fn2, dim3(gx, gy), dim3(fp8q::kEwThreads), 0, stream, yp, xp, bp, gp, rp, rows,
+                  int(cols));
+  return launch(fn1, dim3(gx, gy), dim3(fp8q::kEwThreads), 0, stream, yp, xp, bp, gp, rp, rows,
+                int(cols));
 }
 
 fp8q_status fp8q_token_cat_fp8(uint8_t* q_e4m3, const void* a_bf16, int64_t a_cols,

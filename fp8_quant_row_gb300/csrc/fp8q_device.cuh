@@ -45,6 +45,12 @@ __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t 
   return r;
 }
 
+// Programmatic dependent launch: wait until the grids this launch depends on have completed
+// and their memory is visible (returns at once when there is no such grid).
+__device__ __forceinline__ void wait_for_producers() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Streaming 16-byte global accesses (data touched once).
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }
@@ -160,6 +166,17 @@ __device__ __forceinline__ RowConst row_constants(dd sum, dd sumsq, float cols, 
   return k;
 }
 
+// True when no bf16 value lies within 2^-18 |mu| of the mean, so |x - mu| is never small
+// enough for the absolute error term to matter and the per-element |t| < t_small test can be
+// skipped for the whole row (the usual case: one row in thousands fails this).
+__device__ __forceinline__ bool mean_far_from_bf16_grid(float mu_hi) {
+  const uint32_t u = __float_as_uint(mu_hi);
+  const float lo = __uint_as_float(u & 0xFFFF0000u);            // bf16 value toward zero
+  const float hi = __uint_as_float((u & 0xFFFF0000u) + 0x10000u);  // next bf16 away from zero
+  const float d = fminf(fabsf(__fsub_rn(mu_hi, lo)), fabsf(__fsub_rn(hi, mu_hi)));
+  return d > __fmul_rn(fabsf(mu_hi), 0x1p-18f);
+}
+
 // ------------------------------------------------------------------------------------------
 // normalised value n = RN_bf16((x - mu) * rstd)
 // ------------------------------------------------------------------------------------------
@@ -175,9 +192,12 @@ __device__ __forceinline__ float norm_fast(float x, const RowConst& k) {
   return __fmaf_rn(__fsub_rn(x, k.mu_hi), k.r_hi, k.c);
 }
 
+__device__ __forceinline__ bool near_bf16_midpoint(float t) {
+  return ((__float_as_uint(t) << 16) + kGuardAdd) <= kGuardMax;
+}
+
 __device__ __forceinline__ bool norm_uncertain(float t, const RowConst& k) {
-  const uint32_t g = (__float_as_uint(t) << 16) + kGuardAdd;
-  return (g <= kGuardMax) | (fabsf(t) < k.t_small);
+  return near_bf16_midpoint(t) | (fabsf(t) < k.t_small);
 }
 
 // Exact path: t = (x - mu) * r in double-float, then RN_bf16 of (t_hi + t_lo): t_hi decides
@@ -258,6 +278,19 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
 // bf16x2 word -> (lo, hi) fp32 pair.
 __device__ __forceinline__ f2 bf2_to_f2(uint32_t u) { return f2_make(bf_lo(u), bf_hi(u)); }
 
+// Dekker FastTwoSum on both lanes: s + e == a + b exactly when exponent(a) >= exponent(b).
+__device__ __forceinline__ void fast_two_sum2(f2 a, f2 b, f2& s, f2& e) {
+  s = add2(a, b);
+  e = sub2(b, sub2(s, a));
+}
+
+// Lane-wise max of two packed u16 pairs.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // Knuth TwoSum on both lanes: s + e == a + b exactly.
 __device__ __forceinline__ void two_sum2(f2 a, f2 b, f2& s, f2& e) {
   s = add2(a, b);
@@ -279,6 +312,15 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// 16-byte shared-memory load kept as one instruction (four fp32 lanes).
+__device__ __forceinline__ float4 lds128(const float4* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");

@@ -182,6 +182,59 @@ __device__ __forceinline__ dd dd_norm(float hi, float lo) {
   return r;
 }
 
+// Offsets of the row-sum accumulators from the warp's largest bf16 exponent field mexp
+// (max|x| < 2^(mexp - 126)): K = 2^(mexp - 118) >= 256 max|x|, K2 = 2^(2 mexp - 245) >=
+// 128 max x^2, kept inside the normal fp32 range (K2 = 2^-126 covers every row whose squares
+// are below 2^-133; rows with |x| >= 2^60 are outside the supported range).
+struct RowOffsets {
+  float K, K2;
+  int ek, ek2;  // unbiased exponents of K and K2
+};
+
+__device__ __forceinline__ RowOffsets row_offsets(uint32_t mexp) {
+  const int fk = min(int(mexp) + 9, 254);
+  const int fk2 = min(max(2 * int(mexp) - 118, 1), 254);
+  return RowOffsets{__uint_as_float(uint32_t(fk) << 23), __uint_as_float(uint32_t(fk2) << 23),
+                    fk - 127, fk2 - 127};
+}
+
+// 2^e as a float for e in [-126, 127].
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(uint32_t(e + 127) << 23); }
+
+// x * 2^e in two exact power-of-two steps (no intermediate overflow for |e| <= 250).
+__device__ __forceinline__ float scale2(float x, int e) {
+  const int e1 = e / 2;
+  return __fmul_rn(__fmul_rn(x, pow2f(e1)), pow2f(e - e1));
+}
+
+// Exact warp sum of offset accumulators. Each lane holds two FastTwoSum accumulators
+// s = K + (partial sum), all within [K/2, 2K) (unsigned: [K, 2K)), and the sum of their exact
+// rounding errors e. s - K is an integer number of units u = 2^(ek - 24) (ulp below K; the
+// ulp above K is 2u), read off the bit patterns; the errors are rounded to units of 2^(ek-43)
+// (well below the errors' own fp32 rounding). Both integer totals are reduced with
+// redux.sync (exact, within int32 by the bounds on K) and combined into a double-float.
+__device__ __forceinline__ dd warp_sum_offset(f2 s, f2 e, float K, int ek, bool signed_terms) {
+  const int kb = int(__float_as_uint(K));
+  auto units = [&](float v) -> int {
+    const int d = int(__float_as_uint(v)) - kb;
+    return signed_terms ? (d >= 0 ? 2 * d : d) : d;
+  };
+  // unsigned terms (squares): s in [K, 2K) and the unit is the ulp of K itself
+  const int shift = signed_terms ? 24 : 23;
+  const int u = units(f2_lo(s)) + units(f2_hi(s));
+  const float el = __fadd_rn(f2_lo(e), f2_hi(e));
+  const int ue = __float2int_rn(scale2(el, 43 - ek));
+  const int U = int(__reduce_add_sync(0xffffffffu, uint32_t(u)));
+  const int UE = int(__reduce_add_sync(0xffffffffu, uint32_t(ue)));
+  // total = U * 2^(ek - shift) + UE * 2^(ek - 43) = T * 2^(ek - 43), T exact in int64
+  const long long T = (static_cast<long long>(U) << (43 - shift)) + UE;
+  const float hi = __ll2float_rn(T);
+  const float lo = __ll2float_rn(T - __float2ll_rz(hi));  // exact: |T - hi| < 2^24
+  dd r;
+  two_sum(scale2(hi, ek - 43), scale2(lo, ek - 43), r.hi, r.lo);
+  return r;
+}
+
 // Exact-path fix-up of one 8-element chunk (rare: called only when some element of the chunk
 // is uncertain). Out of line so that the hot loop stays small.
 __device__ __noinline__ uint4 fix_uncertain8(const uint4 x, const uint4 n, const RowConst kc) {
@@ -195,6 +248,49 @@ __device__ __noinline__ uint4 fix_uncertain8(const uint4 x, const uint4 n, const
     nw[i] = lo | (hi << 16);
   }
   return make_uint4(nw[0], nw[1], nw[2], nw[3]);
+}
+
+// n, y and q for the warp's part of one row: chunk j of this lane is stage[j*32], its
+// modulation constants tab[(j*P + 0..3)*32]. kSmallTest adds the per-element |t| < t_small
+// test (rows whose mean lies close to a bf16 value).
+template <int V, int P, bool kSmallTest>
+__device__ __forceinline__ void row_outputs(const uint4* stage, const float4* tab,
+                                            const RowConst& kc, f2 mu2, f2 r2, f2 c2, f2 inv2,
+                                            uint4* yr, uint2* qr) {
+#pragma unroll 2
+  for (int j = 0; j < V; ++j) {
+    const uint4 xv = stage[j * 32];
+    const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
+    uint32_t n[4];
+    bool any = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const f2 tt = fma2(sub2(bf2_to_f2(w4[i]), mu2), r2, c2);
+      const float t0 = f2_lo(tt), t1 = f2_hi(tt);
+      any |= near_bf16_midpoint(t0) | near_bf16_midpoint(t1);
+      if (kSmallTest) any |= (fabsf(t0) < kc.t_small) | (fabsf(t1) < kc.t_small);
+      n[i] = pack_bf16x2(t0, t1);
+    }
+    uint4 nv = make_uint4(n[0], n[1], n[2], n[3]);
+    if (any) nv = fix_uncertain8(xv, nv, kc);
+    const float4 o0 = lds128(tab + (j * P + 0) * 32), o1 = lds128(tab + (j * P + 1) * 32);
+    const float4 h0 = lds128(tab + (j * P + 2) * 32), h1 = lds128(tab + (j * P + 3) * 32);
+    const uint32_t nn[4] = {nv.x, nv.y, nv.z, nv.w};
+    const f2 ops[4] = {f2_make(o0.x, o0.y), f2_make(o0.z, o0.w), f2_make(o1.x, o1.y),
+                       f2_make(o1.z, o1.w)};
+    const f2 shs[4] = {f2_make(h0.x, h0.y), f2_make(h0.z, h0.w), f2_make(h1.x, h1.y),
+                       f2_make(h1.z, h1.w)};
+    uint32_t yw[4], qw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const f2 yf = fma2(bf2_to_f2(nn[i]), ops[i], shs[i]);
+      yw[i] = pack_bf16x2(f2_lo(yf), f2_hi(yf));
+      const f2 qf = mul2(bf2_to_f2(yw[i]), inv2);
+      qw[i] = pack_e4m3x2(f2_lo(qf), f2_hi(qf));
+    }
+    st_stream(yr + j * 32, make_uint4(yw[0], yw[1], yw[2], yw[3]));
+    st_stream(qr + j * 32, make_uint2(qw[0] | (qw[1] << 16), qw[2] | (qw[3] << 16)));
+  }
 }
 
 template <int V, int WPR, bool RESID, bool HAS_BIAS>
@@ -215,6 +311,7 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
   const int row_slot = warp / WPR, part = warp % WPR;
   const RowBlock blk = cta_rows(p.rows, p.mod_rows, n_mod, blockIdx.x, gridDim.x);
   if (blk.begin >= blk.end) return;  // uniform across the CTA
+  wait_for_producers();
   unsigned char* my_ring = ring + size_t(warp) * kStages * L::kStageBytes;
 
   // Row r's part for this warp -> ring stage (each lane copies exactly the chunks it reads).
@@ -288,8 +385,8 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
 #pragma unroll 2
       for (int j = 0; j < V; ++j) {
         const uint4 xv = stage[j * 32], rv = stage[(PC / 8) + j * 32];
-        const float4 gf = tab[(j * P + 4) * 32];
-        const float4 bf = tab[(j * P + 5) * 32];
+        const float4 gf = lds128(tab + (j * P + 4) * 32);
+        const float4 bf = lds128(tab + (j * P + 5) * 32);
         uint4 o;
         o.x = resid2<HAS_BIAS>(xv.x, __float_as_uint(bf.x), __float_as_uint(gf.x), rv.x);
         o.y = resid2<HAS_BIAS>(xv.y, __float_as_uint(bf.y), __float_as_uint(gf.y), rv.y);
@@ -300,8 +397,23 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
       }
     }
 
-    // Row sums, error-free per element (TwoSum on both halves of each bf16 pair).
-    f2 sx = f2_make(0.0f, 0.0f), ex = sx, sq = sx, eq = sx;
+    // Row sums sum(x) and sum(x^2), error-free per element. The accumulators start at powers
+    // of two K (sum) and K2 (squares) above anything a lane's partial sums can reach
+    // (K >= 256 max|x|, K2 >= 128 max x^2 over the warp's part of the row), so every addition
+    // satisfies FastTwoSum's exponent condition and its rounding error is exact; the errors
+    // are accumulated separately. v*v is exact (8-bit significands). max|x| comes from a
+    // packed max over the raw bf16 magnitudes, reduced over the warp.
+    uint32_t m2 = 0;
+#pragma unroll 4
+    for (int j = 0; j < V; ++j) {
+      const uint4 xv = stage[j * 32];
+      m2 = max_u16x2(m2, max_u16x2(xv.x & 0x7FFF7FFFu, xv.y & 0x7FFF7FFFu));
+      m2 = max_u16x2(m2, max_u16x2(xv.z & 0x7FFF7FFFu, xv.w & 0x7FFF7FFFu));
+    }
+    const uint32_t mexp = __reduce_max_sync(0xffffffffu, (max(m2 & 0xFFFFu, m2 >> 16) >> 7) & 0xFFu);
+    const RowOffsets off = row_offsets(mexp);
+    f2 sx = f2_make(off.K, off.K), sq = f2_make(off.K2, off.K2), ex = f2_make(0.0f, 0.0f),
+       eq = ex;
 #pragma unroll 2
     for (int j = 0; j < V; ++j) {
       const uint4 xv = stage[j * 32];
@@ -310,17 +422,16 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
       for (int i = 0; i < 4; ++i) {
         const f2 v = bf2_to_f2(w4[i]);
         f2 s, e;
-        two_sum2(sx, v, s, e);
+        fast_two_sum2(sx, v, s, e);
         sx = s;
         ex = add2(ex, e);
-        two_sum2(sq, mul2(v, v), s, e);  // v*v exact: 8-bit significands
+        fast_two_sum2(sq, mul2(v, v), s, e);
         sq = s;
         eq = add2(eq, e);
       }
     }
-    dd s1 = dd_add(dd_norm(f2_lo(sx), f2_lo(ex)), dd_norm(f2_hi(sx), f2_hi(ex)));
-    dd s2 = dd_add(dd_norm(f2_lo(sq), f2_lo(eq)), dd_norm(f2_hi(sq), f2_hi(eq)));
-    warp_reduce_dd(s1, s2);
+    dd s1 = warp_sum_offset(sx, ex, off.K, off.ek, true);
+    dd s2 = warp_sum_offset(sq, eq, off.K2, off.ek2, false);
     if constexpr (WPR > 1) {
       float4* buf = red + parity * nw + row_slot * WPR;
       if (lane == 0) buf[part] = make_float4(s1.hi, s1.lo, s2.hi, s2.lo);
@@ -342,39 +453,10 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
 
     uint4* yr = reinterpret_cast<uint4*>(p.y + row_off) + lane;
     uint2* qr = reinterpret_cast<uint2*>(p.q + row_off) + lane;
-#pragma unroll 1
-    for (int j = 0; j < V; ++j) {
-      const uint4 xv = stage[j * 32];
-      const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
-      uint32_t n[4];
-      bool any = false;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const f2 tt = fma2(sub2(bf2_to_f2(w4[i]), mu2), r2, c2);
-        const float t0 = f2_lo(tt), t1 = f2_hi(tt);
-        any |= norm_uncertain(t0, kc) | norm_uncertain(t1, kc);
-        n[i] = pack_bf16x2(t0, t1);
-      }
-      uint4 nv = make_uint4(n[0], n[1], n[2], n[3]);
-      if (any) nv = fix_uncertain8(xv, nv, kc);
-      const float4 o0 = tab[(j * P + 0) * 32], o1 = tab[(j * P + 1) * 32];
-      const float4 h0 = tab[(j * P + 2) * 32], h1 = tab[(j * P + 3) * 32];
-      const uint32_t nn[4] = {nv.x, nv.y, nv.z, nv.w};
-      const f2 ops[4] = {f2_make(o0.x, o0.y), f2_make(o0.z, o0.w), f2_make(o1.x, o1.y),
-                         f2_make(o1.z, o1.w)};
-      const f2 shs[4] = {f2_make(h0.x, h0.y), f2_make(h0.z, h0.w), f2_make(h1.x, h1.y),
-                         f2_make(h1.z, h1.w)};
-      uint32_t yw[4], qw[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const f2 yf = fma2(bf2_to_f2(nn[i]), ops[i], shs[i]);
-        yw[i] = pack_bf16x2(f2_lo(yf), f2_hi(yf));
-        const f2 qf = mul2(bf2_to_f2(yw[i]), inv2);
-        qw[i] = pack_e4m3x2(f2_lo(qf), f2_hi(qf));
-      }
-      st_stream(yr + j * 32, make_uint4(yw[0], yw[1], yw[2], yw[3]));
-      st_stream(qr + j * 32, make_uint2(qw[0] | (qw[1] << 16), qw[2] | (qw[3] << 16)));
-    }
+    if (mean_far_from_bf16_grid(kc.mu_hi))
+      row_outputs<V, P, false>(stage, tab, kc, mu2, r2, c2, inv2, yr, qr);
+    else
+      row_outputs<V, P, true>(stage, tab, kc, mu2, r2, c2, inv2, yr, qr);
   }
   cp_async_wait<0>();
 }
@@ -389,6 +471,7 @@ __global__ void __launch_bounds__(kNssThreads) nss_generic_kernel(const NssParam
   __shared__ float4 red[kNssWarps];
   const int chunks = p.cols / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  wait_for_producers();
   const float inv = __frcp_rn(__ldg(p.input_scale));
   const float colsf = float(p.cols);
 
