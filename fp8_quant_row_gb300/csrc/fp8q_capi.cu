@@ -149,6 +149,7 @@ fp8q_status launch_tuned(const fp8q::NssParams& p, const DeviceInfo& dev, int64_
   while (nw >= WPR && L::smem_bytes(nw) > size_t(dev.smem_optin)) nw -= WPR;
   nw -= nw % WPR;
   if (nw < WPR) return FP8Q_OK;
+  if (fp8q::kMaxTableUnitsPerThread * nw * 32 < WPR * V * 32) return FP8Q_OK;
   const size_t smem = L::smem_bytes(nw);
   int bps = 0;
   fp8q_status st = blocks_per_sm(reinterpret_cast<const void*>(fn), nw * 32, smem, &bps);

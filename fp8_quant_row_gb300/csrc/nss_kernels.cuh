@@ -135,6 +135,7 @@ __device__ __forceinline__ void modulate_quant8(const uint4& n, const float* ops
 // ------------------------------------------------------------------------------------------
 
 constexpr int kTunedMaxThreads = 512;
+constexpr int kMaxTableUnitsPerThread = 4;  // the host guarantees 4 * threads >= table units
 constexpr int kStages = 2;
 
 // Shared memory of the tuned kernel: [table | ring | exchange].
@@ -328,26 +329,36 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
     }
   };
 
-  int64_t r = blk.begin + row_slot;
-  if (r < blk.end) issue(r, 0);
-  cp_async_commit();
-
-  // Modulation table of this CTA's group, built while the first rows are in flight.
-  {
-    const size_t mrow = size_t(blk.mod) * C;
-    constexpr int kUnits = WPR * V * 32;
-#pragma unroll 1
-    for (int u = threadIdx.x; u < kUnits; u += blockDim.x) {
+  // Modulation table of this CTA's group, built and published (barrier) before any row copy
+  // is issued: a warp's row copies can stall under memory back-pressure while the first wave
+  // drains, and the barrier must not wait for that.
+  const size_t mrow = size_t(blk.mod) * C;
+  constexpr int kUnits = WPR * V * 32;  // one unit = one (part, chunk, lane): 8 columns
+  constexpr int kRaw = RESID ? 4 : 2;
+  uint4 traw[kMaxTableUnitsPerThread][kRaw];
+#pragma unroll
+  for (int h = 0; h < kMaxTableUnitsPerThread; ++h) {
+    const int u = h * blockDim.x + threadIdx.x;
+    if (u < kUnits) {
       const int l = u & 31, jw = u >> 5;  // jw = w*V + j
       const size_t col = size_t(jw / V) * PC + size_t((jw % V) * 32 + l) * 8;
-      const uint4 sc = __ldg(reinterpret_cast<const uint4*>(p.scale + mrow + col));
-      const uint4 sh = __ldg(reinterpret_cast<const uint4*>(p.shift + mrow + col));
-      uint4 g = make_uint4(0, 0, 0, 0), b = g;
+      traw[h][0] = __ldg(reinterpret_cast<const uint4*>(p.scale + mrow + col));
+      traw[h][1] = __ldg(reinterpret_cast<const uint4*>(p.shift + mrow + col));
       if constexpr (RESID) {
-        g = __ldg(reinterpret_cast<const uint4*>(p.gate + mrow + col));
-        if (HAS_BIAS) b = __ldg(reinterpret_cast<const uint4*>(p.bias + col));
+        traw[h][2] = __ldg(reinterpret_cast<const uint4*>(p.gate + mrow + col));
+        traw[h][3] = HAS_BIAS ? __ldg(reinterpret_cast<const uint4*>(p.bias + col))
+                              : make_uint4(0, 0, 0, 0);
       }
+    }
+  }
+
+#pragma unroll
+  for (int h = 0; h < kMaxTableUnitsPerThread; ++h) {
+    const int u = h * blockDim.x + threadIdx.x;
+    if (u < kUnits) {
+      const int l = u & 31, jw = u >> 5;
       float4* t = table + size_t(jw) * P * 32 + l;
+      const uint4 sc = traw[h][0], sh = traw[h][1];
       t[0 * 32] = make_float4(__fadd_rn(1.0f, bf_lo(sc.x)), __fadd_rn(1.0f, bf_hi(sc.x)),
                               __fadd_rn(1.0f, bf_lo(sc.y)), __fadd_rn(1.0f, bf_hi(sc.y)));
       t[1 * 32] = make_float4(__fadd_rn(1.0f, bf_lo(sc.z)), __fadd_rn(1.0f, bf_hi(sc.z)),
@@ -355,6 +366,7 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
       t[2 * 32] = make_float4(bf_lo(sh.x), bf_hi(sh.x), bf_lo(sh.y), bf_hi(sh.y));
       t[3 * 32] = make_float4(bf_lo(sh.z), bf_hi(sh.z), bf_lo(sh.w), bf_hi(sh.w));
       if constexpr (RESID) {
+        const uint4 g = traw[h][2], b = traw[h][3];
         t[4 * 32] = make_float4(__uint_as_float(g.x), __uint_as_float(g.y), __uint_as_float(g.z),
                                 __uint_as_float(g.w));
         t[5 * 32] = make_float4(__uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z),
@@ -364,6 +376,10 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
   }
   __syncthreads();
 
+  int64_t r = blk.begin + row_slot;
+  if (r < blk.end) issue(r, 0);
+  cp_async_commit();
+
   const float inv = __frcp_rn(__ldg(p.input_scale));
   const f2 inv2 = f2_make(inv, inv);
   const float colsf = float(C);
@@ -372,10 +388,12 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
 
 #pragma unroll 1
   for (int k = 0; r < blk.end; ++k, r += rows_per_iter) {
+    // Wait for row r, then prefetch the next row into the other stage (after, not before:
+    // the first wave of copies then carries only first rows, which arrive sooner).
+    cp_async_wait<0>();  // this lane's copies of row r have landed
     const int64_t rn = r + rows_per_iter;
     if (rn < blk.end) issue(rn, (k + 1) & 1);
     cp_async_commit();
-    cp_async_wait<1>();  // this lane's copies of row r have landed
     const size_t row_off = size_t(r) * C + size_t(part) * PC;
     uint4* stage = reinterpret_cast<uint4*>(my_ring + (k & 1) * L::kStageBytes) + lane;
 
