@@ -152,9 +152,11 @@ struct TunedLayout {
   static constexpr int kPieces = RESID ? 6 : 4;
   static constexpr int kTableF4 = WPR * V * kPieces * 32;
   static constexpr int kStageBytes = kPartCols * 2 * (RESID ? 2 : 1);
+  // + one float4 of row-claim state: the CTA's next-row counter and, with two or more warps
+  // per row, the row each warp group claimed last
   static constexpr size_t smem_bytes(int nw) {
     return size_t(kTableF4) * 16 + size_t(nw) * kStages * kStageBytes +
-           (WPR > 1 ? size_t(2 * nw) * 16 : 0);
+           (WPR > 1 ? size_t(2 * nw) * 16 : 0) + 16 + size_t(nw / WPR) * 4;
   }
 };
 
@@ -307,6 +309,8 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
   const int rows_per_iter = nw / WPR;
   unsigned char* ring = smem_raw + size_t(L::kTableF4) * 16;
   float4* red = reinterpret_cast<float4*>(ring + size_t(nw) * kStages * L::kStageBytes);
+  int* claim = reinterpret_cast<int*>(red + (WPR > 1 ? 2 * nw : 0));  // [0]: counter
+  int* claimed = claim + 4;                                            // per warp group
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row_slot = warp / WPR, part = warp % WPR;
@@ -328,6 +332,8 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
       for (int j = 0; j < V; ++j) cp_async16(dst + (PC / 8) + j * 32, src2 + j * 32);
     }
   };
+
+  if (threadIdx.x == 0) claim[0] = rows_per_iter;  // rows [begin, begin + rows_per_iter) are static
 
   // Modulation table of this CTA's group, built and published (barrier) before any row copy
   // is issued: a warp's row copies can stall under memory back-pressure while the first wave
@@ -387,11 +393,22 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
   int parity = 0;
 
 #pragma unroll 1
-  for (int k = 0; r < blk.end; ++k, r += rows_per_iter) {
-    // Wait for row r, then prefetch the next row into the other stage (after, not before:
-    // the first wave of copies then carries only first rows, which arrive sooner).
+  for (int k = 0; r < blk.end; ++k) {
+    // Wait for row r, then claim the CTA's next unprocessed row and prefetch it into the other
+    // stage. Claiming when the current row has landed balances the rows among the warps:
+    // a warp whose first row arrived late takes fewer of the remaining rows. The first wave
+    // of copies carries only first rows, which therefore arrive sooner.
     cp_async_wait<0>();  // this lane's copies of row r have landed
-    const int64_t rn = r + rows_per_iter;
+    int64_t rn;
+    if constexpr (WPR == 1) {
+      int c = 0;
+      if (lane == 0) c = atomicAdd(claim, 1);
+      rn = blk.begin + __shfl_sync(0xffffffffu, c, 0);
+    } else {
+      if (part == 0 && lane == 0) claimed[row_slot] = atomicAdd(claim, 1);
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + row_slot), "r"(32 * WPR) : "memory");
+      rn = blk.begin + claimed[row_slot];
+    }
     if (rn < blk.end) issue(rn, (k + 1) & 1);
     cp_async_commit();
     const size_t row_off = size_t(r) * C + size_t(part) * PC;
@@ -443,7 +460,10 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
         fast_two_sum2(sx, v, s, e);
         sx = s;
         ex = add2(ex, e);
-        fast_two_sum2(sq, mul2(v, v), s, e);
+        // s = RN(sq + v*v) with v*v exact; its rounding error is v*v + (sq - s), exact
+        // under the same exponent condition, obtained with one more FMA
+        s = fma2(v, v, sq);
+        e = fma2(v, v, sub2(sq, s));
         sq = s;
         eq = add2(eq, e);
       }
@@ -475,6 +495,7 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
       row_outputs<V, P, false>(stage, tab, kc, mu2, r2, c2, inv2, yr, qr);
     else
       row_outputs<V, P, true>(stage, tab, kc, mu2, r2, c2, inv2, yr, qr);
+    r = rn;
   }
   cp_async_wait<0>();
 }
