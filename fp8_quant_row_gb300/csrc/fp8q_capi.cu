@@ -184,7 +184,12 @@ fp8q_status dispatch_ln(const fp8q::NssParams& p, const DeviceInfo& dev, int64_t
                         cudaStream_t stream) {
   bool launched = false;
   fp8q_status st = FP8Q_OK;
-  if (p.cols == 3072)
+  // One warp per row at 3072 (the row is 96 elements per lane); two warps per row for the
+  // residual variant, whose ring stages hold two rows' worth of input (x and residual): half
+  // rows per warp let twice as many warps fit in shared memory.
+  if (p.cols == 3072 && RESID)
+    st = launch_tuned<6, 2, RESID, HAS_BIAS>(p, dev, n_mod, stream, &launched);
+  else if (p.cols == 3072)
     st = launch_tuned<12, 1, RESID, HAS_BIAS>(p, dev, n_mod, stream, &launched);
   else if (p.cols == 6144)
     st = launch_tuned<12, 2, RESID, HAS_BIAS>(p, dev, n_mod, stream, &launched);
