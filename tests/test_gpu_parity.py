@@ -47,6 +47,8 @@ def check_ln(y_gpu, q_gpu, y_ref, q_ref, input_scale, what=""):
     inv = oracle.recip_f32(input_scale)
     assert np.array_equal(q_gpu, oracle.quantize_array(G.bf16_as_f32(y_gpu), inv)), \
         f"{what}: quantise stage not bit-exact on the GPU's own y"
+    from tests.conftest import PARITY_COUNTS
+    PARITY_COUNTS.append((what, nmis, int(y_gpu.size)))
     return nmis
 
 
