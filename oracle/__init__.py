@@ -73,6 +73,18 @@ def _load():
         lib.orc_ln_row_t.restype = None
         lib.orc_nss_fp8.argtypes = [u16p, u8p, u16p, u16p, u16p, i64, f32, i64, i64, f32, f64p]
         lib.orc_nss_fp8.restype = ctypes.c_int
+        lib.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_e2m1_decode.restype = ctypes.c_double
+        lib.orc_e2m1_encode.argtypes = [f32]
+        lib.orc_e2m1_encode.restype = ctypes.c_uint8
+        lib.orc_e2m1_encode_n.argtypes = [ctypes.POINTER(f32), u8p, i64]
+        lib.orc_e2m1_encode_n.restype = None
+        lib.orc_nvfp4_group.argtypes = [u16p, f32, u8p]
+        lib.orc_nvfp4_group.restype = ctypes.c_uint8
+        lib.orc_nvfp4_sf_offset.argtypes = [i64, i64, i64]
+        lib.orc_nvfp4_sf_offset.restype = i64
+        lib.orc_token_cat_nvfp4.argtypes = [u8p, u8p, u16p, i64, u16p, i64, f32, i64]
+        lib.orc_token_cat_nvfp4.restype = ctypes.c_int
         lib.orc_bias_mul_add.argtypes = [u16p, u16p, u16p, u16p, u16p, i64, i64]
         lib.orc_bias_mul_add.restype = ctypes.c_int
         lib.orc_scale_residual_nss_fp8.argtypes = [u16p, u16p, u8p, u16p, u16p, u16p, u16p, u16p,
@@ -202,6 +214,40 @@ def quantize_array(v, inv) -> np.ndarray:
     return out
 
 
+def e2m1_decode(c: int) -> float:
+    return _load().orc_e2m1_decode(int(c) & 0xFF)
+
+
+def e2m1_encode(v) -> int:
+    return _load().orc_e2m1_encode(float(np.float32(v)))
+
+
+def e2m1_encode_array(v) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _load().orc_e2m1_encode_n(_ptr(v, ctypes.c_float), _ptr(out, ctypes.c_uint8), v.size)
+    return out
+
+
+def nvfp4_group(x16, g) -> tuple[int, np.ndarray]:
+    """One 16-element group: (E4M3 block-scale code, 8 packed E2M1 bytes)."""
+    x, xp = _u16(x16)
+    assert x.size == 16
+    packed = np.zeros(8, np.uint8)
+    code = _load().orc_nvfp4_group(xp, float(np.float32(g)), _ptr(packed, ctypes.c_uint8))
+    return code, packed
+
+
+def nvfp4_sf_offset(m: int, k: int, k_groups: int) -> int:
+    return _load().orc_nvfp4_sf_offset(int(m), int(k), int(k_groups))
+
+
+def nvfp4_sf_shape(rows: int, cols: int) -> tuple[int, int]:
+    """(padded rows, padded groups) of the 128x4-tiled block-scale buffer."""
+    k = cols // 16
+    return (rows + 127) // 128 * 128, (k + 3) // 4 * 4
+
+
 # ---- whole operations ------------------------------------------------------------------------
 
 def nss_fp8(x, scale, shift, input_scale, mod_rows=0, eps=1e-6):
@@ -268,3 +314,21 @@ def token_cat_fp8(a, m, input_scale):
     _load().orc_token_cat_fp8(_ptr(q, ctypes.c_uint8), ap, a_cols, mp, m_cols,
                               float(np.float32(input_scale)), rows)
     return q
+
+
+def token_cat_nvfp4(a, m, global_scale):
+    """(q, sf): q [rows, cols/2] packed E2M1 of cat(a[r], m[r]) per 16-element group, sf the
+    128x4-tiled E4M3 block scales (flat, padded rows/groups zero)."""
+    a, ap = _u16(a)
+    m, mp = _u16(m)
+    rows, a_cols = a.shape
+    m_cols = m.shape[1]
+    assert m.shape[0] == rows and (a_cols + m_cols) % 16 == 0
+    cols = a_cols + m_cols
+    mp_, kp_ = nvfp4_sf_shape(rows, cols)
+    q = np.empty((rows, cols // 2), np.uint8)
+    sf = np.empty(mp_ * kp_, np.uint8)
+    rc = _load().orc_token_cat_nvfp4(_ptr(q, ctypes.c_uint8), _ptr(sf, ctypes.c_uint8), ap, a_cols,
+                                     mp, m_cols, float(np.float32(global_scale)), rows)
+    assert rc == 0
+    return q, sf

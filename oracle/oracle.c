@@ -1,8 +1,8 @@
 /*
  * oracle.c -- plain CPU oracle for the row-wise DiT-block prologue:
  *   LayerNorm (no affine) -> AdaLN modulate -> static per-tensor FP8 E4M3 quantisation,
- * and its three variants (gated scale-residual with input bias, deferred output-bias
- * epilogue, token-concat -> FP8).
+ * and its variants (gated scale-residual with input bias, deferred output-bias epilogue,
+ * token-concat -> FP8, token-concat -> NVFP4).
  *
  * TEST INFRASTRUCTURE ONLY. This file is the correctness reference that the CUDA path is
  * compared against. Only the tests, the smoke check and the benchmark's CPU-baseline leg may
@@ -26,6 +26,13 @@
  *  [FLUX-FP8] "sglang #37162 - FLUX.2 FP8 LayerNorm/quant/QKV fusions",
  *             "implementation breakdown" item 4 and "key source snippets"
  *             (_token_cat_fp8_kernel excerpt: cat(attention, mlp) * (1/scale), clamp, cast).
+ *  [FLUX-FP4] "sglang #37141 - FLUX.2 token-cat + NVFP4 fusion", "features and motivation"
+ *             (attention 6144 + MLP 18432 BF16 -> NVFP4 without the concat) and
+ *             "implementation breakdown" items 1-3 (per-group conversion primitive,
+ *             128x4-swizzled block-scale offsets, input_scale_inv as the global scale).
+ *  [NVFP4]    the public NVFP4 format: E2M1 elements (values 0, 0.5, 1, 1.5, 2, 3, 4, 6),
+ *             one E4M3 scale per 16 consecutive elements of a row, an fp32 per-tensor scale;
+ *             and the public 128x4 block-scale tile layout of the FP4 GEMMs that consume it.
  *
  * Parity pins: every function below is pinned by tests/test_oracle_pins.py against
  * something other than itself (exact rational arithmetic, torch's float8/bfloat16 casts,
@@ -393,6 +400,122 @@ ORC_API int orc_token_cat_fp8(uint8_t *q, const uint16_t *a, int64_t a_cols, con
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* Token-concat -> NVFP4                                                                 */
+/* ------------------------------------------------------------------------------------ */
+
+/* Value of an E2M1 code [NVFP4]: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa;
+ * exponent field 0 is subnormal (m * 0.5). Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+ORC_API double orc_e2m1_decode(uint8_t c)
+{
+    const int ef = (c >> 1) & 3, m = c & 1;
+    const double v = ef == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, ef - 1);
+    return (c & 8) ? -v : v;
+}
+
+/*
+ * Saturating round-to-nearest-even encode to E2M1: magnitudes at or above 6 give 6; below,
+ * the nearest of the eight magnitudes, a tie going to the code with mantissa bit 0. The
+ * sign bit is the sign of v, also when the magnitude rounds to 0 (-0.1 -> 0x8). E2M1 has no
+ * NaN: a NaN input gives 0 here and is outside the operation's contract.
+ */
+ORC_API uint8_t orc_e2m1_encode(float v)
+{
+    if (isnan(v))
+        return 0;
+    const uint8_t sign = signbit(v) ? 8 : 0;
+    const double a = fabs((double)v);
+    if (a >= 6.0)
+        return sign | 7;
+    uint8_t best = 0; /* below 6 every distance is exact in fp64 */
+    for (uint8_t c = 1; c < 8; ++c) { /* magnitudes ascend with the code */
+        const double d_best = fabs(a - orc_e2m1_decode(best));
+        const double d_c = fabs(a - orc_e2m1_decode(c));
+        if (d_c < d_best || (d_c == d_best && (c & 1) == 0))
+            best = c;
+    }
+    return sign | best;
+}
+
+/*
+ * One 16-element group [NVFP4; FLUX-FP4 implementation breakdown item 1]. Reading of the
+ * conversion step, in IEEE fp32 with every operation correctly rounded:
+ *   amax  = max |x_i|                                   (exact)
+ *   s     = RN(g * RN(amax * RN(1/6)))                  block scale before encoding
+ *   code  = E4M3_satfinite(s)                           stored block scale
+ *   out   = code == +-0 ? 0 : RN(1 / RN(E4M3(code) * RN(1/g)))
+ *   e_i   = E2M1_satfinite(RN(x_i * out))
+ * g is the per-tensor global scale (the GEMM's input_scale_inv). Element 2j goes to the
+ * low nibble of byte j, element 2j+1 to the high nibble. Returns the scale code.
+ */
+ORC_API uint8_t orc_nvfp4_group(const uint16_t *x, float g, uint8_t *packed)
+{
+    double amax = 0.0;
+    for (int i = 0; i < 16; ++i) {
+        const double a = fabs(orc_bf16_to_f64(x[i]));
+        if (a > amax)
+            amax = a;
+    }
+    const float inv6 = 1.0f / 6.0f;
+    const float s = g * ((float)amax * inv6);
+    const uint8_t code = orc_e4m3_encode(s);
+    float out = 0.0f;
+    if ((code & 0x7F) != 0) {
+        const float inv_g = 1.0f / g;
+        const float d = (float)orc_e4m3_decode(code) * inv_g;
+        out = 1.0f / d;
+    }
+    for (int j = 0; j < 8; ++j) {
+        const uint8_t lo = orc_e2m1_encode((float)orc_bf16_to_f64(x[2 * j]) * out);
+        const uint8_t hi = orc_e2m1_encode((float)orc_bf16_to_f64(x[2 * j + 1]) * out);
+        packed[j] = (uint8_t)(lo | (hi << 4));
+    }
+    return code;
+}
+
+/*
+ * Byte offset of block scale (m, k) -- row m, 16-element group k of K groups per row -- in
+ * the 128x4-tiled layout [FLUX-FP4 implementation breakdown item 1: 128x4 swizzled scale
+ * offsets]: rows are padded to a multiple of 128 and groups to a multiple of 4; each
+ * 128-row x 4-group tile is one 512-byte block, blocks ordered row-tile-major then
+ * group-tile; inside a block, tile row t (0..127) and tile column c (0..3) sit at byte
+ * (t mod 32) * 16 + (t div 32) * 4 + c.
+ */
+ORC_API int64_t orc_nvfp4_sf_offset(int64_t m, int64_t k, int64_t K)
+{
+    const int64_t k_tiles = (K + 3) / 4;
+    const int64_t t = m % 128, c = k % 4;
+    return ((m / 128) * k_tiles + k / 4) * 512 + (t % 32) * 16 + (t / 32) * 4 + c;
+}
+
+/*
+ * Token-concat -> NVFP4 [FLUX-FP4 features and motivation; implementation breakdown items
+ * 1-3]: the row r of cat(a, m) (a_cols + m_cols wide, a multiple of 16) is quantised group by
+ * group with orc_nvfp4_group, without forming the concatenation. q is [rows, cols/2] packed
+ * bytes; sf is the padded 128x4-tiled scale buffer of ceil(rows/128)*128 x ceil(K/4)*4 bytes,
+ * K = cols/16, whose padding entries (rows >= rows, groups >= K) are 0.
+ */
+ORC_API int orc_token_cat_nvfp4(uint8_t *q, uint8_t *sf, const uint16_t *a, int64_t a_cols,
+                                const uint16_t *m, int64_t m_cols, float g, int64_t rows)
+{
+    const int64_t cols = a_cols + m_cols;
+    if (cols % 16 != 0)
+        return 1;
+    const int64_t K = cols / 16;
+    const int64_t m_pad = (rows + 127) / 128 * 128, k_pad = (K + 3) / 4 * 4;
+    memset(sf, 0, (size_t)(m_pad * k_pad));
+    uint16_t grp[16];
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t k = 0; k < K; ++k) {
+            for (int i = 0; i < 16; ++i) {
+                const int64_t c = 16 * k + i;
+                grp[i] = c < a_cols ? a[r * a_cols + c] : m[r * m_cols + (c - a_cols)];
+            }
+            sf[orc_nvfp4_sf_offset(r, k, K)] = orc_nvfp4_group(grp, g, q + r * (cols / 2) + 8 * k);
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* Array forms of the scalar stages (same functions, looped; used by the pin tests)       */
 /* ------------------------------------------------------------------------------------ */
 
@@ -431,4 +554,10 @@ ORC_API void orc_quantize_n(const float *v, float inv, uint8_t *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
         out[i] = orc_quantize(v[i], inv);
+}
+
+ORC_API void orc_e2m1_encode_n(const float *v, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e2m1_encode(v[i]);
 }

@@ -175,3 +175,59 @@ def bf16_product_ties():
             if low > 0 and p % (1 << low) == (1 << (low - 1)):
                 out.append((m1, m2))
     return out
+
+
+@lru_cache(maxsize=1)
+def _e2m1_table():
+    """Non-negative E2M1 values from the format definition: 1 sign bit, 2 exponent bits with
+    bias 1, 1 mantissa bit, exponent field 0 subnormal; no infinities or NaN."""
+    vals, codes = [], []
+    for c in range(0, 8):
+        e, m = (c >> 1) & 3, c & 1
+        v = Fraction(m, 2) if e == 0 else (1 + Fraction(m, 2)) * Fraction(2) ** (e - 1)
+        vals.append(v)
+        codes.append(c)
+    return vals, codes
+
+
+def e2m1_value(c: int) -> Fraction:
+    vals, _ = _e2m1_table()
+    v = vals[c & 7]
+    return -v if c & 8 else v
+
+
+def nearest_e2m1_satfinite(v: float) -> int:
+    """Saturating RNE of a finite float to E2M1 by nearest-value search with exact
+    distances; the sign bit follows the sign of v (so -0.1 and -0.0 give 0x8)."""
+    vals, codes = _e2m1_table()
+    sign = 8 if math.copysign(1.0, v) < 0 else 0
+    a = abs(Fraction(v))
+    if a >= vals[-1]:
+        return sign | codes[-1]
+    i = bisect.bisect_left(vals, a)
+    if vals[i] == a:
+        return sign | codes[i]
+    lo, hi = i - 1, i
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    if dlo < dhi:
+        pick = lo
+    elif dhi < dlo:
+        pick = hi
+    else:
+        pick = lo if codes[lo] % 2 == 0 else hi
+    return sign | codes[pick]
+
+
+def blocked_scale_positions(m_pad: int, k_pad: int) -> np.ndarray:
+    """Position of every (row, group) block scale in the 128x4-tiled layout, built by array
+    reshapes rather than by an offset formula: the padded [m_pad, k_pad] scale matrix is cut
+    into 128x4 tiles (row-tile-major), each tile's 128 rows are split as 4 bands of 32 and
+    stored as 32 lines of 16 bytes (line = row within its band; a line holds the 4 bands
+    side by side, 4 groups each). Returns pos[m, k]."""
+    ids = np.arange(m_pad * k_pad, dtype=np.int64).reshape(m_pad, k_pad)
+    t = ids.reshape(m_pad // 128, 4, 32, k_pad // 4, 4)  # (row tile, band, line, group tile, c)
+    t = t.transpose(0, 3, 2, 1, 4)                        # (row tile, group tile, line, band, c)
+    stored = t.reshape(-1)                                # stored[p] = id of the scale at p
+    pos = np.empty(m_pad * k_pad, np.int64)
+    pos[stored] = np.arange(stored.size)
+    return pos.reshape(m_pad, k_pad)

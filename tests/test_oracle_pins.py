@@ -488,3 +488,188 @@ def test_token_cat_is_quantised_concat():
     inv = oracle.recip_f32(0.1)
     ref = _torch_satfinite_e4m3((torch.from_numpy(v) * torch.tensor(inv)).numpy())
     assert np.array_equal(q, ref)
+
+
+# ------------------------------------------------------------------------------------------
+# Token-concat -> NVFP4
+# ------------------------------------------------------------------------------------------
+
+def test_e2m1_decode_matches_format_definition():
+    for c in range(16):
+        assert Fraction(oracle.e2m1_decode(c)) == exact.e2m1_value(c), c
+        assert math.copysign(1.0, oracle.e2m1_decode(c)) == (-1.0 if c & 8 else 1.0)
+    assert [oracle.e2m1_decode(c) for c in range(8)] == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+
+
+def _e2m1_probe_values(rng):
+    grid = [float(exact.e2m1_value(c)) for c in range(8)]
+    mids = [(a + b) / 2 for a, b in zip(grid, grid[1:])]
+    vals = grid + mids + [6.5, 7.0, 1e30, 3.4e38, 1e-30, 0.0]
+    for v in mids + grid[1:]:
+        vals += [float(np.nextafter(np.float32(v), np.float32(0))),
+                 float(np.nextafter(np.float32(v), np.float32(np.inf)))]
+    vals += list(rng.uniform(0, 8, 2000).astype(np.float32))
+    vals += list((2.0 ** rng.uniform(-12, 4, 2000)).astype(np.float32))
+    vals = np.array(vals, np.float32)
+    return np.concatenate([vals, -vals, np.array([-0.0], np.float32)])
+
+
+def test_e2m1_encode_matches_exact_nearest_search():
+    v = _e2m1_probe_values(np.random.default_rng(7))
+    got = oracle.e2m1_encode_array(v)
+    want = np.array([exact.nearest_e2m1_satfinite(float(x)) for x in v], np.uint8)
+    assert np.array_equal(got, want)
+    # spot values of the tie rule and of saturation, from the definition
+    for x, c in [(0.25, 0x0), (0.75, 0x2), (1.25, 0x2), (1.75, 0x4), (2.5, 0x4), (3.5, 0x6),
+                 (5.0, 0x6), (5.01, 0x7), (1e9, 0x7), (-0.2, 0x8), (-0.0, 0x8), (-5.0, 0xE)]:
+        assert oracle.e2m1_encode(x) == c, (x, c)
+
+
+def test_nvfp4_sf_offset_matches_hand_worked_layout():
+    g = json.load(open(os.path.join(GOLDEN, "nvfp4_sf_layout.json")))
+    for m, k, kk, off in g["cases"]:
+        assert oracle.nvfp4_sf_offset(m, k, kk) == off, (m, k, kk)
+
+
+@pytest.mark.parametrize("rows,groups", [(1, 4), (128, 4), (129, 6), (300, 12), (256, 1)])
+def test_nvfp4_sf_offset_matches_reshape_construction(rows, groups):
+    m_pad, k_pad = oracle.nvfp4_sf_shape(rows, 16 * groups)
+    pos = exact.blocked_scale_positions(m_pad, k_pad)
+    got = np.array([[oracle.nvfp4_sf_offset(m, k, groups) for k in range(k_pad)]
+                    for m in range(m_pad)])
+    assert np.array_equal(got, pos)
+    assert sorted(got.ravel()) == list(range(m_pad * k_pad))  # a permutation of the buffer
+
+
+def _group_bits(vals):
+    return np.array([bf(v) for v in vals], np.uint16)
+
+
+def _unpack(packed):
+    out = []
+    for b in packed:
+        out += [int(b) & 0xF, int(b) >> 4]
+    return out
+
+
+@pytest.mark.parametrize("e", [-6, -3, 0, 2, 8])
+def test_nvfp4_group_is_exact_on_representable_groups(e):
+    # Every element an E2M1 value times 2^e with amax 6 * 2^e and global scale 1: the block
+    # scale must come out as 2^e and every element as its own E2M1 code (closed form).
+    rng = np.random.default_rng(100 + e)
+    codes = rng.integers(0, 16, 16)
+    codes[rng.integers(0, 16)] = 7
+    vals = [float(exact.e2m1_value(int(c))) * 2.0 ** e for c in codes]
+    code, packed = oracle.nvfp4_group(_group_bits(vals), 1.0)
+    assert Fraction(exact.e4m3_value(code)) == Fraction(2) ** e
+    got = _unpack(packed)
+    for c, g_ in zip(codes, got):
+        assert exact.e2m1_value(g_) == exact.e2m1_value(int(c))  # -0 and +0 both allowed only if equal
+
+
+def test_nvfp4_group_nibble_order_and_zero_groups():
+    code, packed = oracle.nvfp4_group(_group_bits([6.0, 0.0] + [0.0] * 14), 1.0)
+    assert code == 0x38 and packed[0] == 0x07 and not packed[1:].any()  # element 0 low nibble
+    code, packed = oracle.nvfp4_group(_group_bits([0.0, -6.0] + [0.0] * 14), 1.0)
+    assert code == 0x38 and packed[0] == 0xF0
+    code, packed = oracle.nvfp4_group(_group_bits([0.0] * 16), 3.0)
+    assert code == 0 and not packed.any()
+    code, packed = oracle.nvfp4_group(np.full(16, 0x8000, np.uint16), 3.0)   # all -0
+    assert code == 0 and (packed == 0x88).all()
+    # block scale below half the smallest E4M3 subnormal: code 0, every element a signed zero
+    code, packed = oracle.nvfp4_group(_group_bits([1e-4, -1e-4] * 8), 1.0)
+    assert code == 0 and (packed == 0x80).all()
+
+
+def _exact_group(xbits, g):
+    """Brute-force evaluation of the group reading with exact rationals and nearest-value
+    searches (tests/exact.py); shares no rounding code with the oracle."""
+    g = np.float32(g)
+    xs = [exact.bf16_value(int(b)) for b in xbits]
+    amax = max(abs(Fraction(x)) for x in xs)
+    inv6 = exact.nearest_f32(Fraction(1, 6))
+    s = exact.nearest_f32(Fraction(float(g)) * Fraction(exact.nearest_f32(amax * Fraction(inv6))))
+    code = exact.nearest_e4m3_satfinite(Fraction(s))
+    if code & 0x7F == 0:
+        out = 0.0
+    else:
+        inv_g = exact.nearest_f32(1 / Fraction(float(g)))
+        d = exact.nearest_f32(Fraction(exact.e4m3_value(code)) * Fraction(inv_g))
+        out = exact.nearest_f32(1 / Fraction(d))
+    elems = []
+    for x in xs:
+        p = Fraction(x) * Fraction(out)
+        v = exact.nearest_f32(p) if p != 0 else math.copysign(0.0, x) * (1.0 if out >= 0 else -1.0)
+        elems.append(exact.nearest_e2m1_satfinite(v))
+    return code, elems
+
+
+def test_nvfp4_group_matches_exact_brute_force():
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        scale_exp = rng.uniform(-8, 8)
+        x = (rng.standard_normal(16) * 2.0 ** scale_exp).astype(np.float32)
+        if trial % 7 == 0:
+            x[rng.integers(0, 16)] *= 40.0         # an outlier sets the block scale
+        g = np.float32(2.0 ** rng.uniform(-4, 12))
+        if trial % 11 == 0:
+            g = np.float32(2688.0 / 7.5)            # a typical input_scale_inv
+        bits = _group_bits(x)
+        code, packed = oracle.nvfp4_group(bits, g)
+        want_code, want_elems = _exact_group(bits, g)
+        assert code == want_code, trial
+        assert _unpack(packed) == want_elems, trial
+
+
+def test_nvfp4_group_amax_element_lands_on_six():
+    # Invariant of the format: with a normal, unsaturated block scale (relative rounding
+    # error <= 2^-4), amax * out lies within [6/(1+2^-4), 6/(1-2^-4)], which rounds to 6.
+    rng = np.random.default_rng(12)
+    hits = 0
+    for _ in range(2000):
+        x = (rng.standard_normal(16) * 2.0 ** rng.uniform(-6, 6)).astype(np.float32)
+        g = np.float32(2.0 ** rng.uniform(-3, 6))
+        bits = _group_bits(x)
+        code, packed = oracle.nvfp4_group(bits, g)
+        if not (0x08 <= code <= 0x7D):          # normal and below the 448 clamp
+            continue
+        xv = np.array([exact.bf16_value(int(b)) for b in bits])
+        i = int(np.argmax(np.abs(xv)))
+        e = _unpack(packed)[i]
+        assert e & 7 == 7, (code, xv[i])
+        hits += 1
+        # every element dequantises within half an E2M1 step (x the block scale) of x
+        dq = np.array([float(exact.e2m1_value(c)) for c in _unpack(packed)])
+        unit = float(exact.e4m3_value(code)) / float(g)
+        assert np.all(np.abs(dq * unit - xv) <= 1.0 * unit * 1.07 + 1e-30)
+    assert hits > 1500
+
+
+def test_nvfp4_group_saturates_the_block_scale():
+    x = _group_bits([1000.0] + [1.0] * 15)
+    code, packed = oracle.nvfp4_group(x, 1000.0)    # s = 1000 * 1000 / 6 >> 448
+    assert code == 0x7E
+    assert _unpack(packed)[0] == 7
+
+
+@pytest.mark.parametrize("rows,a_cols,m_cols", [(5, 48, 80), (130, 40, 88), (128, 64, 64),
+                                                (1, 16, 16)])
+def test_token_cat_nvfp4_is_grouped_concat(rows, a_cols, m_cols):
+    rng = np.random.default_rng(rows + a_cols)
+    a = np.array([bf(v) for v in rng.standard_normal(rows * a_cols)], np.uint16).reshape(rows, a_cols)
+    m = np.array([bf(v) for v in 3 * rng.standard_normal(rows * m_cols)], np.uint16).reshape(rows, m_cols)
+    g = np.float32(2688.0 / 12.0)
+    q, sf = oracle.token_cat_nvfp4(a, m, g)
+    cols = a_cols + m_cols
+    K = cols // 16
+    m_pad, k_pad = oracle.nvfp4_sf_shape(rows, cols)
+    pos = exact.blocked_scale_positions(m_pad, k_pad)
+    cat = np.concatenate([a, m], axis=1)
+    seen = np.zeros(sf.size, bool)
+    for r in range(rows):
+        for k in range(K):
+            code, packed = oracle.nvfp4_group(cat[r, 16 * k:16 * k + 16], g)
+            assert sf[pos[r, k]] == code
+            assert np.array_equal(q[r, 8 * k:8 * k + 8], packed)
+            seen[pos[r, k]] = True
+    assert not sf[~seen].any()          # padding rows and groups hold zero scales

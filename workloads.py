@@ -40,6 +40,10 @@ CONFIGS = {
                      input_scale=0.02, seed=0),
     "token_cat_flux": dict(op="token_cat_fp8", rows=4608, a_cols=6144, m_cols=18432,
                            input_scale=0.1, seed=0),
+    # Same activations quantised to NVFP4; global scale = 448 * 6 / 44.8, the amax that the
+    # FP8 configuration's input_scale 0.1 stands for.
+    "token_cat_nvfp4_flux": dict(op="token_cat_nvfp4", rows=4608, a_cols=6144, m_cols=18432,
+                                 global_scale=60.0, seed=0),
 }
 
 
@@ -109,6 +113,6 @@ def config_inputs(name: str, rows: int | None = None, seed: int | None = None):
                           outlier_gain=c.get("outlier_gain", 20.0))
     if c["op"] in ("scale_residual_nss_fp8", "bias_mul_add"):
         return residual_inputs(r, c["cols"], seed=s)
-    if c["op"] == "token_cat_fp8":
+    if c["op"] in ("token_cat_fp8", "token_cat_nvfp4"):
         return token_cat_inputs(r, c["a_cols"], c["m_cols"], seed=s)
     raise KeyError(name)
