@@ -196,102 +196,144 @@ def make_cases(torch, fq, lib, l2):
     return cases
 
 
-def extra_cases(torch, lib, l2):
+def extra_cases(torch, lib, l2, only=None):
+    """The per-kernel cases: all of them, or only the one named `only`."""
     import workloads as W
 
-    cases = {}
     sh_ = lambda: torch.cuda.current_stream().cuda_stream
 
-    # scale-residual with bias (Qwen-Image)
-    c = W.CONFIGS["scale_residual_qwen"]
-    inp = W.config_inputs("scale_residual_qwen")
-    R, C = inp["x"].shape
-    per = R * C * 9
-    n = n_sets_for(per, l2)
-    bufs = [dict(x=dev_bf16(torch, inp["x"]), r=dev_bf16(torch, inp["residual"]),
-                 ro=torch.empty(R, C, dtype=torch.bfloat16, device="cuda"),
-                 y=torch.empty(R, C, dtype=torch.bfloat16, device="cuda"),
-                 q=torch.empty(R, C, dtype=torch.uint8, device="cuda")) for _ in range(n)]
-    vec = {k: dev_bf16(torch, inp[k]) for k in ("bias", "gate", "scale", "shift")}
-    s = torch.tensor([c["input_scale"]], dtype=torch.float32, device="cuda")
+    def scale_residual_qwen():
+        c = W.CONFIGS["scale_residual_qwen"]
+        inp = W.config_inputs("scale_residual_qwen")
+        R, C = inp["x"].shape
+        per = R * C * 9
+        n = n_sets_for(per, l2)
+        bufs = [dict(x=dev_bf16(torch, inp["x"]), r=dev_bf16(torch, inp["residual"]),
+                     ro=torch.empty(R, C, dtype=torch.bfloat16, device="cuda"),
+                     y=torch.empty(R, C, dtype=torch.bfloat16, device="cuda"),
+                     q=torch.empty(R, C, dtype=torch.uint8, device="cuda")) for _ in range(n)]
+        vec = {k: dev_bf16(torch, inp[k]) for k in ("bias", "gate", "scale", "shift")}
+        s = torch.tensor([c["input_scale"]], dtype=torch.float32, device="cuda")
 
-    def sr(i, bufs=bufs, vec=vec, s=s, R=R, C=C):
-        b = bufs[i % len(bufs)]
-        st = lib.fp8q_scale_residual_nss_fp8(
-            b["ro"].data_ptr(), b["y"].data_ptr(), b["q"].data_ptr(), b["x"].data_ptr(),
-            b["r"].data_ptr(), vec["bias"].data_ptr(), vec["gate"].data_ptr(),
-            vec["scale"].data_ptr(), vec["shift"].data_ptr(), 0, s.data_ptr(), R, C, 1e-6, sh_())
-        if st:
-            raise RuntimeError(f"scale_residual status {st}")
+        def sr(i):
+            b = bufs[i % len(bufs)]
+            st = lib.fp8q_scale_residual_nss_fp8(
+                b["ro"].data_ptr(), b["y"].data_ptr(), b["q"].data_ptr(), b["x"].data_ptr(),
+                b["r"].data_ptr(), vec["bias"].data_ptr(), vec["gate"].data_ptr(),
+                vec["scale"].data_ptr(), vec["shift"].data_ptr(), 0, s.data_ptr(), R, C, 1e-6,
+                sh_())
+            if st:
+                raise RuntimeError(f"scale_residual status {st}")
 
-    cases["scale_residual_qwen"] = Case("scale_residual_nss_fp8", sr, n, per, R,
-                                        "scale_residual_nss_fp8_qwen",
-                                        f"x, residual bf16 [{R},{C}] + bias -> residual_out, y, q")
-    cases["scale_residual_qwen"].keep = (bufs, vec, s)
+        case = Case("scale_residual_nss_fp8", sr, n, per, R, "scale_residual_nss_fp8_qwen",
+                    f"x, residual bf16 [{R},{C}] + bias -> residual_out, y, q")
+        case.keep = (bufs, vec, s)
+        return case
 
-    # bias_mul_add on the same tensors
-    per = R * C * 6
-    n = n_sets_for(per, l2)
-    bufs2 = [dict(x=dev_bf16(torch, inp["x"]), r=dev_bf16(torch, inp["residual"]),
-                  y=torch.empty(R, C, dtype=torch.bfloat16, device="cuda")) for _ in range(n)]
-    g0 = dev_bf16(torch, inp["gate"][0])
+    def bias_mul_add_qwen():
+        inp = W.config_inputs("bias_mul_add_qwen")
+        R, C = inp["x"].shape
+        per = R * C * 6
+        n = n_sets_for(per, l2)
+        bufs = [dict(x=dev_bf16(torch, inp["x"]), r=dev_bf16(torch, inp["residual"]),
+                     y=torch.empty(R, C, dtype=torch.bfloat16, device="cuda")) for _ in range(n)]
+        b, g = dev_bf16(torch, inp["bias"]), dev_bf16(torch, inp["gate"][0])
 
-    def bma(i, bufs=bufs2, b=vec["bias"], g=g0, R=R, C=C):
-        d = bufs[i % len(bufs)]
-        st = lib.fp8q_bias_mul_add(d["y"].data_ptr(), d["x"].data_ptr(), b.data_ptr(),
-                                   g.data_ptr(), d["r"].data_ptr(), R, C, sh_())
-        if st:
-            raise RuntimeError(f"bias_mul_add status {st}")
+        def bma(i):
+            d = bufs[i % len(bufs)]
+            st = lib.fp8q_bias_mul_add(d["y"].data_ptr(), d["x"].data_ptr(), b.data_ptr(),
+                                       g.data_ptr(), d["r"].data_ptr(), R, C, sh_())
+            if st:
+                raise RuntimeError(f"bias_mul_add status {st}")
 
-    cases["bias_mul_add_qwen"] = Case("bias_mul_add", bma, n, per, R, "bias_mul_add_qwen",
-                                      f"x, residual bf16 [{R},{C}] -> y bf16")
-    cases["bias_mul_add_qwen"].keep = (bufs2, g0)
+        case = Case("bias_mul_add", bma, n, per, R, "bias_mul_add_qwen",
+                    f"x, residual bf16 [{R},{C}] -> y bf16")
+        case.keep = (bufs, b, g)
+        return case
 
-    # FLUX.2 LayerNorm, width 6144, per-sample modulation
-    c = W.CONFIGS["nss_flux"]
-    inp = W.config_inputs("nss_flux")
-    R, C = inp["x"].shape
-    per = R * C * 5
-    n = n_sets_for(per, l2)
-    bufs3 = [dict(x=dev_bf16(torch, inp["x"]), y=torch.empty(R, C, dtype=torch.bfloat16, device="cuda"),
-                  q=torch.empty(R, C, dtype=torch.uint8, device="cuda")) for _ in range(n)]
-    sc, shf = dev_bf16(torch, inp["scale"]), dev_bf16(torch, inp["shift"])
-    s3 = torch.tensor([c["input_scale"]], dtype=torch.float32, device="cuda")
-    mr = c["mod_rows"]
+    def nss_flux():
+        c = W.CONFIGS["nss_flux"]
+        inp = W.config_inputs("nss_flux")
+        R, C = inp["x"].shape
+        per = R * C * 5
+        n = n_sets_for(per, l2)
+        bufs = [dict(x=dev_bf16(torch, inp["x"]),
+                     y=torch.empty(R, C, dtype=torch.bfloat16, device="cuda"),
+                     q=torch.empty(R, C, dtype=torch.uint8, device="cuda")) for _ in range(n)]
+        sc, shf = dev_bf16(torch, inp["scale"]), dev_bf16(torch, inp["shift"])
+        s = torch.tensor([c["input_scale"]], dtype=torch.float32, device="cuda")
+        mr = c["mod_rows"]
 
-    def nf(i, bufs=bufs3, sc=sc, shf=shf, s=s3, R=R, C=C):
-        d = bufs[i % len(bufs)]
-        st = lib.fp8q_nss_fp8(d["y"].data_ptr(), d["q"].data_ptr(), d["x"].data_ptr(),
-                              sc.data_ptr(), shf.data_ptr(), mr, s.data_ptr(), R, C, 1e-6, sh_())
-        if st:
-            raise RuntimeError(f"nss flux status {st}")
+        def nf(i):
+            d = bufs[i % len(bufs)]
+            st = lib.fp8q_nss_fp8(d["y"].data_ptr(), d["q"].data_ptr(), d["x"].data_ptr(),
+                                  sc.data_ptr(), shf.data_ptr(), mr, s.data_ptr(), R, C, 1e-6,
+                                  sh_())
+            if st:
+                raise RuntimeError(f"nss flux status {st}")
 
-    cases["nss_flux"] = Case("nss_fp8", nf, n, per, R, "nss_fp8_flux",
-                             f"x bf16 [{R},{C}], scale/shift [2,{C}], mod_rows {mr}")
-    cases["nss_flux"].keep = (bufs3, sc, shf, s3)
+        case = Case("nss_fp8", nf, n, per, R, "nss_fp8_flux",
+                    f"x bf16 [{R},{C}], scale/shift [2,{C}], mod_rows {mr}")
+        case.keep = (bufs, sc, shf, s)
+        return case
 
-    # FLUX.2 token-cat -> FP8
-    c = W.CONFIGS["token_cat_flux"]
-    inp = W.config_inputs("token_cat_flux")
-    R, A = inp["a"].shape
-    M = inp["m"].shape[1]
-    per = R * (A + M) * 3
-    n = n_sets_for(per, l2)
-    bufs4 = [dict(a=dev_bf16(torch, inp["a"]), m=dev_bf16(torch, inp["m"]),
-                  q=torch.empty(R, A + M, dtype=torch.uint8, device="cuda")) for _ in range(n)]
-    s4 = torch.tensor([c["input_scale"]], dtype=torch.float32, device="cuda")
+    def token_cat_flux():
+        c = W.CONFIGS["token_cat_flux"]
+        inp = W.config_inputs("token_cat_flux")
+        R, A = inp["a"].shape
+        M = inp["m"].shape[1]
+        per = R * (A + M) * 3
+        n = n_sets_for(per, l2)
+        bufs = [dict(a=dev_bf16(torch, inp["a"]), m=dev_bf16(torch, inp["m"]),
+                     q=torch.empty(R, A + M, dtype=torch.uint8, device="cuda")) for _ in range(n)]
+        s = torch.tensor([c["input_scale"]], dtype=torch.float32, device="cuda")
 
-    def tc(i, bufs=bufs4, s=s4, R=R, A=A, M=M):
-        d = bufs[i % len(bufs)]
-        st = lib.fp8q_token_cat_fp8(d["q"].data_ptr(), d["a"].data_ptr(), A, d["m"].data_ptr(),
-                                    M, s.data_ptr(), R, sh_())
-        if st:
-            raise RuntimeError(f"token_cat status {st}")
+        def tc(i):
+            d = bufs[i % len(bufs)]
+            st = lib.fp8q_token_cat_fp8(d["q"].data_ptr(), d["a"].data_ptr(), A,
+                                        d["m"].data_ptr(), M, s.data_ptr(), R, sh_())
+            if st:
+                raise RuntimeError(f"token_cat status {st}")
 
-    cases["token_cat_flux"] = Case("token_cat_fp8", tc, n, per, R, "token_cat_fp8_flux",
-                                   f"a bf16 [{R},{A}] + m bf16 [{R},{M}] -> q e4m3 [{R},{A + M}]")
-    cases["token_cat_flux"].keep = (bufs4, s4)
-    return cases
+        case = Case("token_cat_fp8", tc, n, per, R, "token_cat_fp8_flux",
+                    f"a bf16 [{R},{A}] + m bf16 [{R},{M}] -> q e4m3 [{R},{A + M}]")
+        case.keep = (bufs, s)
+        return case
+
+    def token_cat_nvfp4_flux():
+        c = W.CONFIGS["token_cat_nvfp4_flux"]
+        inp = W.config_inputs("token_cat_nvfp4_flux")
+        R, A = inp["a"].shape
+        M = inp["m"].shape[1]
+        K = (A + M) // 16
+        sf_bytes = lib.fp8q_nvfp4_scale_bytes(R, A + M)
+        per = R * (A + M) * 2 + R * (A + M) // 2 + sf_bytes
+        n = n_sets_for(per, l2)
+        bufs = [dict(a=dev_bf16(torch, inp["a"]), m=dev_bf16(torch, inp["m"]),
+                     q=torch.empty(R, (A + M) // 2, dtype=torch.uint8, device="cuda"),
+                     sf=torch.empty(sf_bytes, dtype=torch.uint8, device="cuda"))
+                for _ in range(n)]
+        s = torch.tensor([c["global_scale"]], dtype=torch.float32, device="cuda")
+
+        def tc4(i):
+            d = bufs[i % len(bufs)]
+            st = lib.fp8q_token_cat_nvfp4(d["q"].data_ptr(), d["sf"].data_ptr(),
+                                          d["a"].data_ptr(), A, d["m"].data_ptr(), M,
+                                          s.data_ptr(), R, sh_())
+            if st:
+                raise RuntimeError(f"token_cat_nvfp4 status {st}")
+
+        case = Case("token_cat_nvfp4", tc4, n, per, R, "token_cat_nvfp4_flux",
+                    f"a bf16 [{R},{A}] + m bf16 [{R},{M}] -> q e2m1 [{R},{(A + M) // 2}] "
+                    f"bytes + {K} e4m3 block scales per row (128x4 tiles), global scale "
+                    f"{c['global_scale']}")
+        case.keep = (bufs, s)
+        return case
+
+    builders = {"scale_residual_qwen": scale_residual_qwen, "bias_mul_add_qwen": bias_mul_add_qwen,
+                "nss_flux": nss_flux, "token_cat_flux": token_cat_flux,
+                "token_cat_nvfp4_flux": token_cat_nvfp4_flux}
+    return {k: f for k, f in builders.items() if only is None or k == only}
 
 
 def capture(torch, case: Case, count: int, start: int):
@@ -482,15 +524,15 @@ def run_ours(args):
         line["e2e"] = e2e_measure(torch, lib, main, max(3, min(args.steps, 200)))
     if rank == 0 and not args.skip_kernels:
         ks = {}
-        extra = extra_cases(torch, lib, l2)
-        for key, case in extra.items():
+        for key, build_case in extra_cases(torch, lib, l2).items():
+            case = build_case()
             kms, _, _ = time_case(torch, case, 200, 5, use_graph=not args.no_graph)
             per = kms / 200
             ks[key] = {"kernel": case.name, "workload": case.describe,
                        "us_per_launch": round(per * 1e3, 3), "rows_per_s": round(case.rows / (per / 1e3), 1),
                        "roofline": roofline_entry(case, per, peak, peak_src)}
             del case
-        extra.clear()
+            torch.cuda.empty_cache()
         line["kernels"] = ks
     if rank == 0 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -555,7 +597,7 @@ def run_profile_only(args):
     if args.profile_only == "nss_qwen":
         case = make_cases(torch, fq, lib, l2)["nss_qwen"]
     else:
-        case = extra_cases(torch, lib, l2)[args.profile_only]
+        case = extra_cases(torch, lib, l2, only=args.profile_only)[args.profile_only]()
     for i in range(args.warmup + args.steps):
         case.launch(i)
     torch.cuda.synchronize()
@@ -574,6 +616,7 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile-only", choices=("nss_qwen", "scale_residual_qwen",
+                                               "token_cat_nvfp4_flux",
                                                "bias_mul_add_qwen", "nss_flux", "token_cat_flux"),
                     help="only launch this workload (W+K launches, no timing): for ncu captures")
     args = ap.parse_args()

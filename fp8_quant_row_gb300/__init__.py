@@ -9,6 +9,7 @@ library's sm_103a kernels; there is no CPU or eager fallback.
     r, y, q = scale_residual_nss_fp8(x, residual, gate, scale, shift, input_scale, bias=b)
     y = bias_mul_add(x, bias, gate, residual)
     q = token_cat_fp8(attention, mlp, input_scale)
+    q4, sf = token_cat_nvfp4(attention, mlp, global_scale)            # uint8 codes / scales
 """
 from __future__ import annotations
 
@@ -18,7 +19,8 @@ from . import _capi
 from ._build import build
 from ._capi import Fp8qError
 
-__all__ = ["nss_fp8", "scale_residual_nss_fp8", "bias_mul_add", "token_cat_fp8", "build",
+__all__ = ["nss_fp8", "scale_residual_nss_fp8", "bias_mul_add", "token_cat_fp8",
+           "token_cat_nvfp4", "nvfp4_scale_bytes", "build",
            "Fp8qError", "library_path"]
 
 EPS = 1e-6
@@ -121,3 +123,33 @@ def token_cat_fp8(a, m, input_scale, *, q=None, stream=None):
                                         _stream_handle(stream))
     _capi.check(st, "fp8q_token_cat_fp8")
     return q
+
+
+def nvfp4_scale_bytes(rows: int, cols: int) -> int:
+    """Size of the padded 128x4-tiled block-scale buffer for a [rows, cols] NVFP4 tensor."""
+    n = _capi.lib().fp8q_nvfp4_scale_bytes(int(rows), int(cols))
+    if n < 0:
+        raise ValueError(f"no NVFP4 layout for rows={rows}, cols={cols}")
+    return n
+
+
+def token_cat_nvfp4(a, m, global_scale, *, q=None, sf=None, stream=None):
+    """NVFP4 of cat(a, m, dim=-1) without a BF16 concat: (q, sf), both uint8.
+
+    q [..., (a_cols + m_cols) / 2] holds two E2M1 codes per byte (first element in the low
+    nibble); sf is the flat 128x4-tiled E4M3 block-scale buffer (nvfp4_scale_bytes bytes,
+    padding rows zero). global_scale: one-element float32 CUDA tensor (input_scale_inv)."""
+    _bf16(a, "a"), _bf16(m, "m")
+    rows, a_cols = _rows_cols(a)
+    m_cols = m.shape[-1]
+    if m.numel() != rows * m_cols:
+        raise TypeError("a and m must have the same number of rows")
+    cols = a_cols + m_cols
+    q = _out(q, (*a.shape[:-1], cols // 2), torch.uint8, a, "q")
+    n_sf = _capi.lib().fp8q_nvfp4_scale_bytes(rows, cols)
+    sf = _out(sf, (max(n_sf, 0),), torch.uint8, a, "sf")
+    st = _capi.lib().fp8q_token_cat_nvfp4(q.data_ptr(), sf.data_ptr(), a.data_ptr(), a_cols,
+                                          m.data_ptr(), m_cols, _scale_ptr(global_scale), rows,
+                                          _stream_handle(stream))
+    _capi.check(st, "fp8q_token_cat_nvfp4")
+    return q, sf

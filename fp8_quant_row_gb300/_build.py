@@ -12,7 +12,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfp8q.so")
 SOURCES = [os.path.join(CSRC, "fp8q_capi.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fp8q_device.cuh", "nss_kernels.cuh",
-                                                  "elementwise_kernels.cuh")] + \
+                                                  "elementwise_kernels.cuh",
+                                                  "nvfp4_kernels.cuh")] + \
     [os.path.join(INCLUDE, "fp8q.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")

@@ -16,12 +16,14 @@
 #include "fp8q.h"
 #include "elementwise_kernels.cuh"
 #include "nss_kernels.cuh"
+#include "nvfp4_kernels.cuh"
 
 namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxLnCols = 32768;
 constexpr int64_t kMaxEwCols = int64_t(1) << 30;
+constexpr int kFp4UnitsPerThread = 1;  // 64-element units per thread of token_cat_nvfp4
 
 thread_local int g_last_cuda_error = 0;
 thread_local char g_last_detail[160] = "";
@@ -97,6 +99,7 @@ fp8q_status blocks_per_sm(const void* fn, int threads, size_t smem, int* blocks)
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 struct Range {
   const void* p;
@@ -372,11 +375,52 @@ fp8q_status fp8q_token_cat_fp8(uint8_t* q_e4m3, const void* a_bf16, int64_t a_co
                 static_cast<const uint16_t*>(m_bf16), int(m_cols), input_scale, rows);
 }
 
+int64_t fp8q_nvfp4_scale_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 16 || cols % 16 != 0 || cols > kMaxEwCols) return -1;
+  const int64_t groups = cols / 16;
+  return (rows + 127) / 128 * 128 * ((groups + 3) / 4 * 4);
+}
+
+fp8q_status fp8q_token_cat_nvfp4(uint8_t* q_fp4, uint8_t* sf_e4m3, const void* a_bf16,
+                                 int64_t a_cols, const void* m_bf16, int64_t m_cols,
+                                 const float* global_scale, int64_t rows, cudaStream_t stream) {
+  if (rows < 0 || a_cols < 64 || m_cols < 64 || a_cols % 64 != 0 || m_cols % 64 != 0 ||
+      a_cols + m_cols > kMaxEwCols)
+    return FP8Q_ERR_SHAPE;
+  if (rows == 0) return FP8Q_OK;
+  if (!q_fp4 || !sf_e4m3 || !a_bf16 || !m_bf16 || !global_scale) return FP8Q_ERR_NULL;
+  if (!aligned32(q_fp4) || !aligned32(a_bf16) || !aligned32(m_bf16) || !aligned16(sf_e4m3))
+    return FP8Q_ERR_ALIGN;
+  const int64_t cols = a_cols + m_cols;
+  const int64_t rows_pad = (rows + 127) / 128 * 128;
+  const Range q{q_fp4, size_t(rows) * size_t(cols / 2)};
+  const Range sf{sf_e4m3, size_t(fp8q_nvfp4_scale_bytes(rows, cols))};
+  const Range a{a_bf16, size_t(rows) * size_t(a_cols) * 2};
+  const Range m{m_bf16, size_t(rows) * size_t(m_cols) * 2};
+  const Range gs{global_scale, 4};
+  if (overlap(q, a) || overlap(q, m) || overlap(q, gs) || overlap(sf, a) || overlap(sf, m) ||
+      overlap(sf, gs) || overlap(q, sf))
+    return FP8Q_ERR_ALIAS;
+  const DeviceInfo* dev = nullptr;
+  fp8q_status st = current_device(&dev);
+  if (st != FP8Q_OK) return st;
+  const int units = int(cols / 64);
+  const int per_cta = fp8q::kFp4Threads * kFp4UnitsPerThread;
+  const unsigned gy = unsigned((units + per_cta - 1) / per_cta);
+  const unsigned gx = unsigned(rows_pad < 0x7FFFFFFF ? rows_pad : 0x7FFFFFFF);
+  if (gy > 65535u) return FP8Q_ERR_SHAPE;
+  return launch(fp8q::token_cat_nvfp4_kernel<kFp4UnitsPerThread>, dim3(gx, gy),
+                dim3(fp8q::kFp4Threads), 0, stream, q_fp4, sf_e4m3,
+                static_cast<const uint16_t*>(a_bf16), int(a_cols / 64),
+                static_cast<const uint16_t*>(m_bf16), int(m_cols / 64), global_scale, rows,
+                rows_pad);
+}
+
 const char* fp8q_status_string(int status) {
   switch (status) {
     case FP8Q_OK: return "ok";
     case FP8Q_ERR_NULL: return "null pointer";
-    case FP8Q_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case FP8Q_ERR_ALIGN: return "pointer not aligned (16 bytes; 32 for NVFP4 data)";
     case FP8Q_ERR_SHAPE: return "unsupported shape";
     case FP8Q_ERR_UNSUPPORTED: return "device is not compute capability 10.3 (GB300)";
     case FP8Q_ERR_ALIAS: return "an output overlaps an input or another output";

@@ -1,0 +1,155 @@
+// nvfp4_kernels.cuh -- token-concat -> NVFP4 for sm_103a.
+//
+// "sglang #37141 - FLUX.2 token-cat + NVFP4 fusion" (features and motivation; implementation
+// breakdown items 1-3) and the public NVFP4 format (E2M1 elements, one E4M3 scale per 16
+// consecutive elements of a row, an fp32 per-tensor global scale g, scales stored in the
+// 128x4-tiled layout the FP4 GEMMs read). Per 16-element group of the row cat(a[r], m[r]):
+//   amax = max |x_i|
+//   code = E4M3_satfinite(RN(g * RN(amax * RN(1/6))))             stored block scale
+//   out  = code == +-0 ? 0 : RN(1 / RN(E4M3(code) * RN(1/g)))
+//   e_i  = E2M1_satfinite(RN(x_i * out)),  element 2j -> low nibble of byte j
+// All roundings are IEEE fp32 round-to-nearest-even; the BF16 concat is never formed.
+//
+// Work unit: four consecutive groups (64 elements = 128 source bytes) of one part of one row.
+// They are one column of one 128x4 scale tile, so their four scale codes form one aligned
+// 32-bit word of the scale buffer, and their 32 bytes of packed codes one aligned 32-byte
+// store. A thread moves its unit with four 32-byte loads (one 1-KB contiguous access per warp
+// and instruction) and two stores. Grid: x = padded rows (grid-stride past 2^31-1), y = unit
+// blocks of a row; rows past `rows` (the padding of the last 128-row tile) only write zero
+// scale words. `out` depends on the code alone, so each CTA tabulates it for all 256 codes
+// (correctly rounded reciprocals) while its first loads are in flight.
+#pragma once
+
+#include "fp8q_device.cuh"
+
+namespace fp8q {
+
+constexpr int kFp4Threads = 128;
+
+// 32-byte streaming load / store (sm_100+ 256-bit global accesses).
+__device__ __forceinline__ void ld_stream32(const void* p, uint32_t (&w)[8]) {
+  asm volatile("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void st_stream32(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                  "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// Value of an E4M3 code (exact: E4M3 -> f16 -> f32 are both widening).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const uint16_t c = uint16_t(code & 0xFF);
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(uint16_t(h2 & 0xFFFF)));
+  return f;
+}
+
+// Four packed fp32 pairs (elements 0..7 in order) -> eight E2M1 codes, element 0 in bits 0..3.
+// cvt.rn.satfinite.e2m1x2 puts its first source in the high nibble.
+__device__ __forceinline__ uint32_t pack_e2m1x8(f2 p0, f2 p1, f2 p2, f2 p3) {
+  uint32_t r;
+  asm("{\n"
+      ".reg .b8 b0, b1, b2, b3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      "mov.b32 %0, {b0, b1, b2, b3};\n"
+      "}"
+      : "=r"(r)
+      : "f"(f2_lo(p0)), "f"(f2_hi(p0)), "f"(f2_lo(p1)), "f"(f2_hi(p1)), "f"(f2_lo(p2)),
+        "f"(f2_hi(p2)), "f"(f2_lo(p3)), "f"(f2_hi(p3)));
+  return r;
+}
+
+// max |x| of a 16-element group held as eight bf16x2 words, as an fp32 value. |bf16| bit
+// patterns order like their values, so the maximum is an integer max of the magnitudes.
+__device__ __forceinline__ float group_amax(const uint32_t (&w)[8]) {
+  uint32_t m = max_u16x2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu);
+#pragma unroll
+  for (int i = 2; i < 8; ++i) m = max_u16x2(m, w[i] & 0x7FFF7FFFu);
+  const uint32_t lo = m & 0xFFFFu, hi = m >> 16;
+  return __uint_as_float((lo > hi ? lo : hi) << 16);
+}
+
+// The 8 bytes of packed codes of one group, given its output scale.
+__device__ __forceinline__ void quant_group(const uint32_t (&w)[8], float out, uint32_t& lo,
+                                            uint32_t& hi) {
+  const f2 o = f2_make(out, out);
+  lo = pack_e2m1x8(mul2(bf2_to_f2(w[0]), o), mul2(bf2_to_f2(w[1]), o), mul2(bf2_to_f2(w[2]), o),
+                   mul2(bf2_to_f2(w[3]), o));
+  hi = pack_e2m1x8(mul2(bf2_to_f2(w[4]), o), mul2(bf2_to_f2(w[5]), o), mul2(bf2_to_f2(w[6]), o),
+                   mul2(bf2_to_f2(w[7]), o));
+}
+
+// UPT units per thread, unit ku = blockIdx.y * 128 * UPT + threadIdx.x + u * 128.
+// a_units / m_units: units per row of each part (a_cols / 64, m_cols / 64).
+template <int UPT>
+__global__ void __launch_bounds__(kFp4Threads) token_cat_nvfp4_kernel(
+    uint8_t* __restrict__ q, uint8_t* __restrict__ sf, const uint16_t* __restrict__ a,
+    int a_units, const uint16_t* __restrict__ m, int m_units,
+    const float* __restrict__ global_scale, int64_t rows, int64_t rows_pad) {
+  __shared__ float out_of_code[256];
+  const int units = a_units + m_units;  // also the number of 4-group scale tiles per row
+  const int a_cols = a_units * 64, m_cols = m_units * 64;
+  const int ku0 = blockIdx.y * (kFp4Threads * UPT) + threadIdx.x;
+  wait_for_producers();
+  const float g = __ldg(global_scale);
+  const float inv6 = __frcp_rn(6.0f);
+  bool table_ready = false;
+
+  for (int64_t r = blockIdx.x; r < rows_pad; r += gridDim.x) {
+    // byte offset of this row's scale word inside each 512-byte tile of its 128-row band
+    uint8_t* sf_row = sf + size_t(r >> 7) * size_t(units) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+    if (r >= rows) {
+#pragma unroll
+      for (int u = 0; u < UPT; ++u) {
+        const int ku = ku0 + u * kFp4Threads;
+        if (ku < units) *reinterpret_cast<uint32_t*>(sf_row + size_t(ku) * 512) = 0u;
+      }
+      continue;
+    }
+    uint32_t w[UPT][4][8];
+#pragma unroll
+    for (int u = 0; u < UPT; ++u) {
+      const int ku = ku0 + u * kFp4Threads;
+      if (ku < units) {
+        const uint16_t* src = ku < a_units ? a + size_t(r) * a_cols + size_t(ku) * 64
+                                           : m + size_t(r) * m_cols + size_t(ku - a_units) * 64;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ld_stream32(src + 16 * j, w[u][j]);
+      }
+    }
+    if (!table_ready) {  // first row of this CTA: tabulate out(code) behind the loads
+      const float inv_g = __frcp_rn(g);
+      for (int c = threadIdx.x; c < 256; c += kFp4Threads)
+        out_of_code[c] = (c & 0x7F) ? __frcp_rn(__fmul_rn(e4m3_value(c), inv_g)) : 0.0f;
+      __syncthreads();
+      table_ready = true;
+    }
+#pragma unroll
+    for (int u = 0; u < UPT; ++u) {
+      const int ku = ku0 + u * kFp4Threads;
+      if (ku >= units) continue;
+      float s[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[j] = __fmul_rn(g, __fmul_rn(group_amax(w[u][j]), inv6));
+      const uint32_t codes = pack_e4m3x2(s[0], s[1]) | (pack_e4m3x2(s[2], s[3]) << 16);
+      uint32_t packed[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        quant_group(w[u][j], out_of_code[(codes >> (8 * j)) & 0xFF], packed[2 * j],
+                    packed[2 * j + 1]);
+      st_stream32(q + size_t(r) * (size_t(units) * 32) + size_t(ku) * 32, packed);
+      *reinterpret_cast<uint32_t*>(sf_row + size_t(ku) * 512) = codes;
+    }
+  }
+}
+
+}  // namespace fp8q

@@ -6,6 +6,8 @@
  *   scale_residual_nss_fp8  gated residual update (optional input bias), then nss_fp8.
  *   bias_mul_add            deferred output-bias epilogue y = (x + bias) * gate + residual.
  *   token_cat_fp8           E4M3 quantisation of the row concat [a | m] without a BF16 concat.
+ *   token_cat_nvfp4         NVFP4 quantisation (E2M1 codes + 128x4-tiled E4M3 block scales)
+ *                           of the same row concat.
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers to row-major, contiguous arrays on the current
@@ -14,7 +16,8 @@
  *   - The caller owns every buffer. The library allocates nothing, never synchronises and
  *     only enqueues work on `stream` (0 = the legacy default stream). Outputs are complete
  *     when that stream reaches the launch.
- *   - Every tensor pointer must be 16-byte aligned (FP8Q_ERR_ALIGN otherwise).
+ *   - Every tensor pointer must be 16-byte aligned (FP8Q_ERR_ALIGN otherwise); the NVFP4
+ *     entry point needs 32 bytes for its data pointers.
  *   - rows == 0 returns FP8Q_OK without touching any pointer or launching anything.
  *   - Argument errors are reported synchronously, before any launch, with a status code; a
  *     failed launch returns FP8Q_ERR_CUDA (fp8q_last_cuda_error() gives the cudaError_t).
@@ -33,6 +36,12 @@
  *               item 3, key source snippets (bias_mul_add_kernel), review highlights.
  *   [FLUX-FP8]  "sglang #37162 - FLUX.2 FP8 LayerNorm/quant/QKV fusions": implementation
  *               breakdown items 2 and 4, key source snippets (_token_cat_fp8_kernel).
+ *   [FLUX-FP4]  "sglang #37141 - FLUX.2 token-cat + NVFP4 fusion": features and motivation
+ *               (attention 6144 + MLP 18432 -> NVFP4 without the concat), implementation
+ *               breakdown items 1-3 (per-group conversion, 128x4-swizzled scale offsets,
+ *               input_scale_inv as the global scale, 32-byte aligned dense BF16 inputs).
+ *   [NVFP4]     the public NVFP4 format: E2M1 elements, one E4M3 scale per 16 consecutive
+ *               elements of a row, an fp32 per-tensor scale; 128x4 scale tiles of FP4 GEMMs.
  */
 #ifndef FP8Q_H
 #define FP8Q_H
@@ -135,6 +144,42 @@ fp8q_status fp8q_bias_mul_add(void* y_bf16, const void* x_bf16, const void* bias
 fp8q_status fp8q_token_cat_fp8(uint8_t* q_e4m3, const void* a_bf16, int64_t a_cols,
                                const void* m_bf16, int64_t m_cols, const float* input_scale,
                                int64_t rows, cudaStream_t stream);
+
+/*
+ * Token-concat -> NVFP4 [FLUX-FP4; NVFP4]: row r of cat(a, m) is quantised in 16-element
+ * groups straight from the two sources (no BF16 concat). Per group, in IEEE fp32 with every
+ * operation rounded to nearest even:
+ *   amax = max |x_i|
+ *   sf   = E4M3_satfinite(RN(g * RN(amax * RN(1/6))))                 (stored block scale)
+ *   out  = sf == +-0 ? 0 : RN(1 / RN(E4M3(sf) * RN(1/g)))
+ *   e_i  = E2M1_satfinite(RN(x_i * out))          E2M1 magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6
+ * so E2M1(e_i) * E4M3(sf) / g approximates x_i. g = *global_scale (the consuming GEMM's
+ * input_scale_inv; finite and > 0, not checked). Sign of a zero result follows x_i * out.
+ *
+ *   q_fp4        out  [rows, (a_cols + m_cols) / 2] bytes; byte j of a row holds element 2j in
+ *                     bits 0..3 and element 2j+1 in bits 4..7
+ *   sf_e4m3      out  fp8q_nvfp4_scale_bytes(rows, a_cols + m_cols) bytes: block scale of
+ *                     (row r, group k) of K = cols/16 groups at byte
+ *                       ((r / 128) * ceil(K / 4) + k / 4) * 512
+ *                       + (r % 32) * 16 + ((r % 128) / 32) * 4 + k % 4
+ *                     (128-row x 4-group tiles of 512 bytes); entries of padding rows
+ *                     (rows .. ceil(rows/128)*128 - 1) are written with 0
+ *   a_bf16       in   [rows, a_cols] bf16 (attention part)
+ *   m_bf16       in   [rows, m_cols] bf16 (MLP part)
+ *   a_cols, m_cols    multiples of 64, >= 64 (FLUX.2: 6144 and 18432)
+ *   global_scale in   device pointer to one fp32
+ *   Alignment: q_fp4, a_bf16, m_bf16 32-byte aligned; sf_e4m3 16-byte aligned.
+ *   Aliasing: q_fp4, sf_e4m3, a_bf16, m_bf16 and global_scale pairwise disjoint.
+ *   Inputs containing NaN give unspecified codes in their group (no NaN in E2M1).
+ */
+fp8q_status fp8q_token_cat_nvfp4(uint8_t* q_fp4, uint8_t* sf_e4m3, const void* a_bf16,
+                                 int64_t a_cols, const void* m_bf16, int64_t m_cols,
+                                 const float* global_scale, int64_t rows, cudaStream_t stream);
+
+/* Bytes of the padded block-scale buffer of fp8q_token_cat_nvfp4 for a [rows, cols] input:
+ * ceil(rows/128)*128 * ceil(cols/64)*4. -1 for rows < 0 or cols not a positive multiple of 16.
+ * Host-only arithmetic. */
+int64_t fp8q_nvfp4_scale_bytes(int64_t rows, int64_t cols);
 
 /* Human-readable name of a status code (static string; never NULL). */
 const char* fp8q_status_string(int status);

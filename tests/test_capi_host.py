@@ -155,3 +155,31 @@ def test_product_package_never_imports_the_oracle():
             "print(any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules))")
     out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
     assert out.stdout.strip() == "False", out.stderr
+
+
+def test_token_cat_nvfp4_argument_checks(L):
+    def call(q=A, sf=4 * A, a=8 * A, ac=6144, m=16 * A, mc=18432, s=40 * A, rows=4):
+        return L.fp8q_token_cat_nvfp4(q, sf, a, ac, m, mc, s, rows, None)
+    assert call(ac=6144 - 16) == SHAPE       # parts must be multiples of 64 columns
+    assert call(mc=32) == SHAPE
+    assert call(rows=-1) == SHAPE
+    assert call(rows=0, q=None, sf=None) == OK
+    assert call(sf=None) == NULL
+    assert call(s=None) == NULL
+    assert call(a=8 * A + 16) == ALIGN       # 16-byte aligned is not enough for the data
+    assert call(q=A + 16) == ALIGN
+    assert call(sf=4 * A + 8) == ALIGN
+    assert call(sf=8 * A + 64) == ALIAS      # scales inside a
+    assert call(q=16 * A) == ALIAS
+    assert call(sf=A + 32) == ALIAS         # scales inside q
+    assert call(s=4 * A + 4) == ALIAS        # global scale inside the scale buffer
+
+
+def test_nvfp4_scale_bytes(L):
+    f = L.fp8q_nvfp4_scale_bytes
+    assert f(4608, 24576) == 4608 * 1536
+    assert f(17, 24576) == 128 * 1536          # rows padded to 128
+    assert f(1, 16) == 128 * 4                 # groups padded to 4
+    assert f(129, 80) == 256 * 8
+    assert f(0, 64) == 0
+    assert f(-1, 64) == -1 and f(4, 24) == -1 and f(4, 0) == -1

@@ -1,7 +1,8 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle, element by element.
 
 Acceptance (per stage):
-  * bias_mul_add, token_cat_fp8, residual_out: bit-exact.
+  * bias_mul_add, token_cat_fp8, token_cat_nvfp4 (codes and block scales), residual_out:
+    bit-exact.
   * quantise stage: q_gpu == E4M3(RN(y_gpu * inv)) bit-exact for every element (the
     oracle's quantise applied to the GPU's own y).
   * LayerNorm outputs: max |ulp| of y <= 1 against the oracle; q bit-exact wherever y
@@ -283,6 +284,81 @@ def test_token_cat_special_values():
 
 
 # ------------------------------------------------------------------------------------------
+# token_cat_nvfp4
+# ------------------------------------------------------------------------------------------
+
+def run_token_cat_nvfp4(a, m, g):
+    rows = a.shape[0]
+    cols = a.shape[1] + m.shape[1]
+    q = G.Guarded((rows, cols // 2), torch.uint8)
+    sf = G.Guarded((fq().nvfp4_scale_bytes(rows, cols),), torch.uint8)  # canary-filled too
+    fq().token_cat_nvfp4(G.dev_bf16(a), G.dev_bf16(m), G.dev_scale(g), q=q.tensor, sf=sf.tensor)
+    torch.cuda.synchronize()
+    assert q.intact() and sf.intact()
+    return G.host_u8(q.tensor), G.host_u8(sf.tensor)
+
+
+def check_nvfp4(a, m, g, what=""):
+    qg, sg = run_token_cat_nvfp4(a, m, g)
+    qr, sr = oracle.token_cat_nvfp4(a, m, g)
+    assert np.array_equal(sg, sr), f"{what}: block scales differ at {np.nonzero(sg != sr)[0][:8]}"
+    bad = np.nonzero(qg != qr)
+    assert not bad[0].size, f"{what}: codes differ at {list(zip(*bad))[:8]}"
+
+
+def test_token_cat_nvfp4_flux_config_bit_exact():
+    c = W.CONFIGS["token_cat_nvfp4_flux"]
+    inp = W.config_inputs("token_cat_nvfp4_flux")
+    check_nvfp4(inp["a"], inp["m"], c["global_scale"], "flux config")
+
+
+@pytest.mark.parametrize("rows,a_cols,m_cols", [(1, 6144, 18432), (17, 6144, 18432),
+                                                (129, 6144, 18432), (127, 64, 64),
+                                                (5, 64, 1024), (300, 128, 192)])
+def test_token_cat_nvfp4_shapes_and_padding(rows, a_cols, m_cols):
+    inp = W.token_cat_inputs(rows, a_cols, m_cols, seed=rows + 7)
+    for g in (60.0, 1.0, 358.4, 1e-3, 1e6):
+        check_nvfp4(inp["a"], inp["m"], g, f"{rows}x{a_cols}+{m_cols} g={g}")
+
+
+def test_token_cat_nvfp4_special_values_and_ties():
+    """Exact E2M1 midpoints (ties to even), signed zeros, +-Inf, bf16 subnormals and the
+    largest finite bf16, block scales that saturate or vanish."""
+    def bf(v):
+        return int(W.to_bf16_bits(torch.tensor([float(v)]))[0])
+    grid = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    mids = [(x + y) / 2 for x, y in zip(grid, grid[1:])]
+    groups = []
+    for e in (-4, 0, 3):  # amax 6 * 2^e with g = 1 makes the block scale exactly 2^e
+        for sign in (1, -1):
+            vals = [6.0] + [sign * v for v in mids] + [sign * v for v in grid[1:]] + [-0.0]
+            groups.append([bf(v * 2.0 ** e) for v in vals])
+    groups.append([0x7F80, 0xFF80] + [bf(1.0)] * 14)            # +-Inf: scale saturates
+    groups.append([0x7F7F, 0xFF7F] + [0x0001] * 14)             # largest finite, subnormals
+    groups.append([0x8001, 0x0001, 0x8000, 0x0000] * 4)         # scale code 0: signed zeros
+    groups.append([bf(-1e-3)] * 8 + [bf(1e-3)] * 8)
+    groups.append([0x8000] * 16)
+    groups.append([bf(v) for v in np.linspace(-3, 3, 16)])
+    flat = np.array(groups, np.uint16).ravel()
+    flat = np.resize(flat, 4 * 128)  # four rows of 128 = 64 + 64
+    x = flat.reshape(4, 128)
+    for g in (1.0, 0.5, 3.0e4):
+        check_nvfp4(x[:, :64].copy(), x[:, 64:].copy(), g, f"specials g={g}")
+
+
+def test_token_cat_nvfp4_zero_rows_and_repeat_calls_agree():
+    inp = W.token_cat_inputs(256, 6144, 18432, seed=3)
+    a = inp["a"].copy()
+    a[5] = 0
+    a[200] = 0x8000
+    q1, s1 = run_token_cat_nvfp4(a, inp["m"], 60.0)
+    q2, s2 = run_token_cat_nvfp4(a, inp["m"], 60.0)
+    assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
+    qr, sr = oracle.token_cat_nvfp4(a, inp["m"], 60.0)
+    assert np.array_equal(q1, qr) and np.array_equal(s1, sr)
+
+
+# ------------------------------------------------------------------------------------------
 # boundary behaviour on the device
 # ------------------------------------------------------------------------------------------
 
@@ -290,6 +366,7 @@ def test_rows_zero_launches_nothing_and_returns_ok():
     L = fq()._capi.lib()
     assert L.fp8q_nss_fp8(None, None, None, None, None, 0, None, 0, 3072, 1e-6, None) == 0
     assert L.fp8q_token_cat_fp8(None, None, 16, None, 16, None, 0, None) == 0
+    assert L.fp8q_token_cat_nvfp4(None, None, None, 64, None, 64, None, 0, None) == 0
 
 
 def test_errors_are_reported_before_launch():
