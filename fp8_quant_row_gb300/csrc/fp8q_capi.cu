@@ -23,7 +23,6 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxLnCols = 32768;
 constexpr int64_t kMaxEwCols = int64_t(1) << 30;
-constexpr int kFp4UnitsPerThread = 1;  // 64-element units per thread of token_cat_nvfp4
 
 thread_local int g_last_cuda_error = 0;
 thread_local char g_last_detail[160] = "";
@@ -405,13 +404,11 @@ fp8q_status fp8q_token_cat_nvfp4(uint8_t* q_fp4, uint8_t* sf_e4m3, const void* a
   fp8q_status st = current_device(&dev);
   if (st != FP8Q_OK) return st;
   const int units = int(cols / 64);
-  const int per_cta = fp8q::kFp4Threads * kFp4UnitsPerThread;
-  const unsigned gy = unsigned((units + per_cta - 1) / per_cta);
-  const unsigned gx = unsigned(rows_pad < 0x7FFFFFFF ? rows_pad : 0x7FFFFFFF);
-  if (gy > 65535u) return FP8Q_ERR_SHAPE;
-  return launch(fp8q::token_cat_nvfp4_kernel<kFp4UnitsPerThread>, dim3(gx, gy),
-                dim3(fp8q::kFp4Threads), 0, stream, q_fp4, sf_e4m3,
-                static_cast<const uint16_t*>(a_bf16), int(a_cols / 64),
+  const unsigned gx = unsigned((units + fp8q::kFp4UnitsPerCta - 1) / fp8q::kFp4UnitsPerCta);
+  const int64_t groups = rows_pad / 8;  // 8-row groups; the kernel strides over the rest
+  const unsigned gy = unsigned(groups < 65535 ? groups : 65535);
+  return launch(fp8q::token_cat_nvfp4_kernel, dim3(gx, gy), dim3(fp8q::kFp4Threads), 0, stream,
+                q_fp4, sf_e4m3, static_cast<const uint16_t*>(a_bf16), int(a_cols / 64),
                 static_cast<const uint16_t*>(m_bf16), int(m_cols / 64), global_scale, rows,
                 rows_pad);
 }

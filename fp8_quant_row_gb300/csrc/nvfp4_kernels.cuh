@@ -13,18 +13,18 @@
 // Work unit: four consecutive groups (64 elements = 128 source bytes) of one part of one row.
 // They are one column of one 128x4 scale tile, so their four scale codes form one aligned
 // 32-bit word of the scale buffer, and their 32 bytes of packed codes one aligned 32-byte
-// store. A thread moves its unit with four 32-byte loads (one 1-KB contiguous access per warp
-// and instruction) and two stores. Grid: x = padded rows (grid-stride past 2^31-1), y = unit
-// blocks of a row; rows past `rows` (the padding of the last 128-row tile) only write zero
-// scale words. `out` depends on the code alone, so each CTA tabulates it for all 256 codes
-// (correctly rounded reciprocals) while its first loads are in flight.
+// store. A thread moves its unit with four 32-byte loads and one 32-byte store; the scale
+// words of a warp are regrouped by one shuffle into whole 32-byte sectors (see the kernel).
+// Rows past `rows` (the padding of the last 128-row tile) take part with zero scale words.
+// The output scale needs one correctly rounded reciprocal per group.
 #pragma once
 
 #include "fp8q_device.cuh"
 
 namespace fp8q {
 
-constexpr int kFp4Threads = 128;
+constexpr int kFp4Threads = 256;
+constexpr int kFp4UnitsPerCta = 32;  // 8 warps x 4 units, each over the same 8 rows
 
 // 32-byte streaming load / store (sm_100+ 256-bit global accesses).
 __device__ __forceinline__ void ld_stream32(const void* p, uint32_t (&w)[8]) {
@@ -88,67 +88,59 @@ __device__ __forceinline__ void quant_group(const uint32_t (&w)[8], float out, u
                    mul2(bf2_to_f2(w[7]), o));
 }
 
-// UPT units per thread, unit ku = blockIdx.y * 128 * UPT + threadIdx.x + u * 128.
-// a_units / m_units: units per row of each part (a_cols / 64, m_cols / 64).
-template <int UPT>
+// One warp covers 8 rows x 4 units: the rows {t, t+1} + {0, 32, 64, 96} of one 128-row band
+// (t even), whose scale words for one unit fill one aligned 32-byte sector of the scale
+// tile. Lane l takes row j = l / 4 of the group and unit k = l % 4 of the warp's four, so
+// after one shuffle the warp writes four whole sectors with one store instruction, and the
+// L2 never sees a partial-sector scale write. A CTA (8 warps) covers 32 consecutive units
+// of its 8 rows. Grid: x = unit blocks of a row, y = row groups (grid-stride).
 __global__ void __launch_bounds__(kFp4Threads) token_cat_nvfp4_kernel(
     uint8_t* __restrict__ q, uint8_t* __restrict__ sf, const uint16_t* __restrict__ a,
     int a_units, const uint16_t* __restrict__ m, int m_units,
     const float* __restrict__ global_scale, int64_t rows, int64_t rows_pad) {
-  __shared__ float out_of_code[256];
   const int units = a_units + m_units;  // also the number of 4-group scale tiles per row
   const int a_cols = a_units * 64, m_cols = m_units * 64;
-  const int ku0 = blockIdx.y * (kFp4Threads * UPT) + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int j = lane >> 2;                        // row of the group: line parity j & 1, band j >> 1
+  const int ku = blockIdx.x * kFp4UnitsPerCta + (threadIdx.x >> 5) * 4 + (lane & 3);
+  // shuffle source for the sector layout: lane L stores word L & 7 of sector L >> 3, which
+  // holds line parity (L & 7) >> 2 and band (L & 3)
+  const int src_j = ((lane & 3) << 1) | ((lane >> 2) & 1);
+  const int src = src_j * 4 + (lane >> 3);
+  const int st_ku = blockIdx.x * kFp4UnitsPerCta + (threadIdx.x >> 5) * 4 + (lane >> 3);
   wait_for_producers();
   const float g = __ldg(global_scale);
   const float inv6 = __frcp_rn(6.0f);
-  bool table_ready = false;
+  const float inv_g = __frcp_rn(g);
 
-  for (int64_t r = blockIdx.x; r < rows_pad; r += gridDim.x) {
-    // byte offset of this row's scale word inside each 512-byte tile of its 128-row band
-    uint8_t* sf_row = sf + size_t(r >> 7) * size_t(units) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-    if (r >= rows) {
-#pragma unroll
-      for (int u = 0; u < UPT; ++u) {
-        const int ku = ku0 + u * kFp4Threads;
-        if (ku < units) *reinterpret_cast<uint32_t*>(sf_row + size_t(ku) * 512) = 0u;
-      }
-      continue;
-    }
-    uint32_t w[UPT][4][8];
-#pragma unroll
-    for (int u = 0; u < UPT; ++u) {
-      const int ku = ku0 + u * kFp4Threads;
-      if (ku < units) {
-        const uint16_t* src = ku < a_units ? a + size_t(r) * a_cols + size_t(ku) * 64
+  for (int64_t grp = blockIdx.y; grp < rows_pad / 8; grp += gridDim.y) {
+    const int64_t band = grp >> 4;
+    const int t0 = int(grp & 15) * 2;  // even line of the band
+    const int64_t r = band * 128 + (j >> 1) * 32 + t0 + (j & 1);
+    uint32_t codes = 0;
+    if (r < rows && ku < units) {
+      const uint16_t* src_p = ku < a_units ? a + size_t(r) * a_cols + size_t(ku) * 64
                                            : m + size_t(r) * m_cols + size_t(ku - a_units) * 64;
+      uint32_t w[4][8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) ld_stream32(src + 16 * j, w[u][j]);
-      }
-    }
-    if (!table_ready) {  // first row of this CTA: tabulate out(code) behind the loads
-      const float inv_g = __frcp_rn(g);
-      for (int c = threadIdx.x; c < 256; c += kFp4Threads)
-        out_of_code[c] = (c & 0x7F) ? __frcp_rn(__fmul_rn(e4m3_value(c), inv_g)) : 0.0f;
-      __syncthreads();
-      table_ready = true;
-    }
-#pragma unroll
-    for (int u = 0; u < UPT; ++u) {
-      const int ku = ku0 + u * kFp4Threads;
-      if (ku >= units) continue;
+      for (int i = 0; i < 4; ++i) ld_stream32(src_p + 16 * i, w[i]);
       float s[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) s[j] = __fmul_rn(g, __fmul_rn(group_amax(w[u][j]), inv6));
-      const uint32_t codes = pack_e4m3x2(s[0], s[1]) | (pack_e4m3x2(s[2], s[3]) << 16);
+      for (int i = 0; i < 4; ++i) s[i] = __fmul_rn(g, __fmul_rn(group_amax(w[i]), inv6));
+      codes = pack_e4m3x2(s[0], s[1]) | (pack_e4m3x2(s[2], s[3]) << 16);
       uint32_t packed[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        quant_group(w[u][j], out_of_code[(codes >> (8 * j)) & 0xFF], packed[2 * j],
-                    packed[2 * j + 1]);
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t c = (codes >> (8 * i)) & 0xFF;
+        const float out = (c & 0x7F) ? __frcp_rn(__fmul_rn(e4m3_value(c), inv_g)) : 0.0f;
+        quant_group(w[i], out, packed[2 * i], packed[2 * i + 1]);
+      }
       st_stream32(q + size_t(r) * (size_t(units) * 32) + size_t(ku) * 32, packed);
-      *reinterpret_cast<uint32_t*>(sf_row + size_t(ku) * 512) = codes;
     }
+    const uint32_t word = __shfl_sync(0xFFFFFFFFu, codes, src);
+    if (st_ku < units)
+      *reinterpret_cast<uint32_t*>(sf + (size_t(band) * units + st_ku) * 512 + t0 * 16 +
+                                   (lane & 7) * 4) = word;
   }
 }
 
