@@ -85,6 +85,15 @@ def _load():
         lib.orc_nvfp4_sf_offset.restype = i64
         lib.orc_token_cat_nvfp4.argtypes = [u8p, u8p, u16p, i64, u16p, i64, f32, i64]
         lib.orc_token_cat_nvfp4.restype = ctypes.c_int
+        f32p = ctypes.POINTER(f32)
+        lib.orc_rms_norm_head.argtypes = [u16p, u16p, i64, f32, u16p]
+        lib.orc_rms_norm_head.restype = None
+        lib.orc_rope_interleaved.argtypes = [u16p, f32p, i64, u16p]
+        lib.orc_rope_interleaved.restype = None
+        lib.orc_qkv_epilogue.argtypes = [u16p, u16p, u16p, u16p, u16p, u16p, i64, i64,
+                                         u16p, u16p, u16p, i64, i64, u16p, u16p, u16p, u16p,
+                                         f32p, f32p, i64, f32, f32]
+        lib.orc_qkv_epilogue.restype = ctypes.c_int
         lib.orc_bias_mul_add.argtypes = [u16p, u16p, u16p, u16p, u16p, i64, i64]
         lib.orc_bias_mul_add.restype = ctypes.c_int
         lib.orc_scale_residual_nss_fp8.argtypes = [u16p, u16p, u8p, u16p, u16p, u16p, u16p, u16p,
@@ -332,3 +341,53 @@ def token_cat_nvfp4(a, m, global_scale):
                                      mp, m_cols, float(np.float32(global_scale)), rows)
     assert rc == 0
     return q, sf
+
+
+HEAD_DIM = 128
+
+
+def rms_norm_head(x, w, eps=1e-6) -> np.ndarray:
+    """n = RN_bf16(x * w / sqrt(mean(x^2) + eps)) for one head vector (uint16 bf16 bits)."""
+    x, xp = _u16(x)
+    w, wp = _u16(w)
+    assert x.size == w.size
+    out = np.empty(x.size, np.uint16)
+    _load().orc_rms_norm_head(xp, wp, x.size, float(np.float32(eps)), _ptr(out, ctypes.c_uint16))
+    return out
+
+
+def rope_interleaved(n, cos_sin) -> np.ndarray:
+    """Interleaved RoPE of one head vector with an fp32 cache row (cos first, then sin)."""
+    n, np_ = _u16(n)
+    cs = np.ascontiguousarray(cos_sin, dtype=np.float32)
+    assert cs.size == n.size
+    out = np.empty(n.size, np.uint16)
+    _load().orc_rope_interleaved(np_, _ptr(cs, ctypes.c_float), n.size, _ptr(out, ctypes.c_uint16))
+    return out
+
+
+def qkv_epilogue(txt, img, heads):
+    """txt / img: dicts with q, k, v ([tokens, ld] uint16 arrays, head h at columns
+    h*128 .. h*128+127 of each row), wq, wk ([128] uint16), cos_sin ([tokens, 128] float32)
+    and eps. Returns joint (q, k, v), each [t_tokens + i_tokens, heads, 128] uint16."""
+    def prep(st):
+        arrs = {}
+        for key in ("q", "k", "v", "wq", "wk"):
+            arrs[key] = _u16(st[key])
+        cs = np.ascontiguousarray(st["cos_sin"], dtype=np.float32)
+        arrs["cs"] = (cs, _ptr(cs, ctypes.c_float))
+        return arrs
+    t, i = prep(txt), prep(img)
+    tt, it = txt["q"].shape[0], img["q"].shape[0]
+    for st, n in ((txt, tt), (img, it)):
+        assert st["q"].shape[1] >= heads * HEAD_DIM and st["cos_sin"].shape == (n, HEAD_DIM)
+        assert st["q"].shape == st["k"].shape == st["v"].shape
+    out = [np.empty((tt + it, heads, HEAD_DIM), np.uint16) for _ in range(3)]
+    rc = _load().orc_qkv_epilogue(
+        *[_ptr(o, ctypes.c_uint16) for o in out],
+        t["q"][1], t["k"][1], t["v"][1], txt["q"].shape[1], tt,
+        i["q"][1], i["k"][1], i["v"][1], img["q"].shape[1], it,
+        t["wq"][1], t["wk"][1], i["wq"][1], i["wk"][1], t["cs"][1], i["cs"][1], heads,
+        float(np.float32(txt["eps"])), float(np.float32(img["eps"])))
+    assert rc == 0
+    return tuple(out)

@@ -2,7 +2,8 @@
  * oracle.c -- plain CPU oracle for the row-wise DiT-block prologue:
  *   LayerNorm (no affine) -> AdaLN modulate -> static per-tensor FP8 E4M3 quantisation,
  * and its variants (gated scale-residual with input bias, deferred output-bias epilogue,
- * token-concat -> FP8, token-concat -> NVFP4).
+ * token-concat -> FP8, token-concat -> NVFP4), and the attention-input epilogue after the
+ * packed QKV GEMM (per-head Q/K RMSNorm, interleaved RoPE, V copy, joint [text, image] pack).
  *
  * TEST INFRASTRUCTURE ONLY. This file is the correctness reference that the CUDA path is
  * compared against. Only the tests, the smoke check and the benchmark's CPU-baseline leg may
@@ -30,6 +31,12 @@
  *             (attention 6144 + MLP 18432 BF16 -> NVFP4 without the concat) and
  *             "implementation breakdown" items 1-3 (per-group conversion primitive,
  *             128x4-swizzled block-scale offsets, input_scale_inv as the global scale).
+ *  [QWEN-QKV] "sglang #37123 - Qwen-Image FP8 QKV fusion", "implementation breakdown" item 3
+ *             (Q/K RMSNorm + RoPE, V copy, joint [text, image] output; head_dim 128) and
+ *             "key source snippets" (per-stream norm weights and epsilons, per-stream cos/sin
+ *             caches, is_neox=False: interleaved pairs).
+ *  [FLUX-QKV] "sglang #37162 - FLUX.2 FP8 LayerNorm/quant/QKV fusions", "implementation
+ *             breakdown" item 3 (QK RMSNorm, RoPE, QKV pack and text/image concat in one kernel).
  *  [NVFP4]    the public NVFP4 format: E2M1 elements (values 0, 0.5, 1, 1.5, 2, 3, 4, 6),
  *             one E4M3 scale per 16 consecutive elements of a row, an fp32 per-tensor scale;
  *             and the public 128x4 block-scale tile layout of the FP4 GEMMs that consume it.
@@ -512,6 +519,101 @@ ORC_API int orc_token_cat_nvfp4(uint8_t *q, uint8_t *sf, const uint16_t *a, int6
             }
             sf[orc_nvfp4_sf_offset(r, k, K)] = orc_nvfp4_group(grp, g, q + r * (cols / 2) + 8 * k);
         }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* QKV epilogue: per-head RMSNorm + interleaved RoPE, V copy, joint [text, image] pack      */
+/* ------------------------------------------------------------------------------------ */
+
+/*
+ * RMSNorm of one head vector of D BF16 values with a BF16 weight [QWEN-QKV implementation
+ * breakdown item 3: Q/K RMS norm per head]: n_j = RN_bf16(x_j * w_j / sqrt(sum_i x_i^2 / D +
+ * eps)), the exact value rounded once. fp64: the squares of BF16 values are exact, their sum
+ * is exact unless the magnitudes span more than ~2^18, and the one division and square root
+ * are correctly rounded, so the fp64 value is within a few 2^-53 of the exact one.
+ */
+ORC_API void orc_rms_norm_head(const uint16_t *x, const uint16_t *w, int64_t D, float eps,
+                               uint16_t *n)
+{
+    double ss = 0.0;
+    for (int64_t j = 0; j < D; ++j) {
+        const double v = orc_bf16_to_f64(x[j]);
+        ss += v * v;
+    }
+    const double rrms = 1.0 / sqrt(ss / (double)D + (double)eps);
+    for (int64_t j = 0; j < D; ++j)
+        n[j] = orc_bf16_from_f64(orc_bf16_to_f64(x[j]) * orc_bf16_to_f64(w[j]) * rrms);
+}
+
+/*
+ * Interleaved (GPT-J style, is_neox=False) rotary embedding of one head vector [QWEN-QKV key
+ * source snippets]: pair i = (n[2i], n[2i+1]) is rotated by (c_i, s_i) = (cos_sin[i],
+ * cos_sin[D/2 + i]) from the fp32 cache row, each product and the sum rounded to fp32 as
+ * separate operations (no fused multiply-add), then to BF16:
+ *   o[2i]   = RN_bf16(RN32(RN32(n[2i]   * c) - RN32(n[2i+1] * s)))
+ *   o[2i+1] = RN_bf16(RN32(RN32(n[2i+1] * c) + RN32(n[2i]   * s)))
+ */
+ORC_API void orc_rope_interleaved(const uint16_t *n, const float *cos_sin, int64_t D,
+                                  uint16_t *o)
+{
+    for (int64_t i = 0; i < D / 2; ++i) {
+        const float c = cos_sin[i], s = cos_sin[D / 2 + i];
+        const float a = (float)orc_bf16_to_f64(n[2 * i]);
+        const float b = (float)orc_bf16_to_f64(n[2 * i + 1]);
+        const float ac = a * c, bs = b * s, bc = b * c, as = a * s;
+        o[2 * i] = orc_bf16_from_f32(ac - bs);
+        o[2 * i + 1] = orc_bf16_from_f32(bc + as);
+    }
+}
+
+#define ORC_HEAD_DIM 128
+
+/* One stream's Q or K head: RMSNorm then RoPE. */
+static void qk_head(const uint16_t *x, const uint16_t *w, const float *cos_sin, float eps,
+                    uint16_t *out)
+{
+    uint16_t n[ORC_HEAD_DIM];
+    orc_rms_norm_head(x, w, ORC_HEAD_DIM, eps, n);
+    orc_rope_interleaved(n, cos_sin, ORC_HEAD_DIM, out);
+}
+
+/*
+ * The attention-input epilogue [QWEN-QKV implementation breakdown item 3; FLUX-QKV
+ * implementation breakdown item 3]. Two streams (text, image), each with Q, K, V rows of
+ * heads x 128 BF16 values at a row stride of ld elements (the packed GEMM output: Q, K, V
+ * side by side), a cos/sin cache row per token ([tokens, 128] fp32: cos in 0..63, sin in
+ * 64..127) and RMSNorm weights for Q and K ([128] BF16 each) and an eps. Output rows
+ * [t_tokens + i_tokens, heads, 128], text first:
+ *   joint_q[r, h] = RoPE(RMSNorm(q[h], wq), cache[r'])   (r' the token's row in its stream)
+ *   joint_k[r, h] = RoPE(RMSNorm(k[h], wk), cache[r'])
+ *   joint_v[r, h] = v[h]                                   (bit copy)
+ */
+ORC_API int orc_qkv_epilogue(uint16_t *jq, uint16_t *jk, uint16_t *jv,
+                             const uint16_t *tq, const uint16_t *tk, const uint16_t *tv,
+                             int64_t t_ld, int64_t t_tokens,
+                             const uint16_t *iq, const uint16_t *ik, const uint16_t *iv,
+                             int64_t i_ld, int64_t i_tokens,
+                             const uint16_t *twq, const uint16_t *twk, const uint16_t *iwq,
+                             const uint16_t *iwk, const float *t_cs, const float *i_cs,
+                             int64_t heads, float t_eps, float i_eps)
+{
+    const int64_t D = ORC_HEAD_DIM, row = heads * D;
+    for (int64_t r = 0; r < t_tokens + i_tokens; ++r) {
+        const int txt = r < t_tokens;
+        const int64_t rr = txt ? r : r - t_tokens;
+        const int64_t ld = txt ? t_ld : i_ld;
+        const uint16_t *q = (txt ? tq : iq) + rr * ld, *k = (txt ? tk : ik) + rr * ld,
+                       *v = (txt ? tv : iv) + rr * ld;
+        const uint16_t *wq = txt ? twq : iwq, *wk = txt ? twk : iwk;
+        const float *cs = (txt ? t_cs : i_cs) + rr * D;
+        const float eps = txt ? t_eps : i_eps;
+        for (int64_t h = 0; h < heads; ++h) {
+            qk_head(q + h * D, wq, cs, eps, jq + r * row + h * D);
+            qk_head(k + h * D, wk, cs, eps, jk + r * row + h * D);
+            memcpy(jv + r * row + h * D, v + h * D, D * sizeof(uint16_t));
+        }
+    }
     return 0;
 }
 

@@ -673,3 +673,136 @@ def test_token_cat_nvfp4_is_grouped_concat(rows, a_cols, m_cols):
             assert np.array_equal(q[r, 8 * k:8 * k + 8], packed)
             seen[pos[r, k]] = True
     assert not sf[~seen].any()          # padding rows and groups hold zero scales
+
+
+# ------------------------------------------------------------------------------------------
+# QKV epilogue: per-head RMSNorm, interleaved RoPE, joint pack
+# ------------------------------------------------------------------------------------------
+
+def _exact_rms_head(xb, wb, eps):
+    xs = [F(exact.bf16_value(int(b))) for b in xb]
+    ws = [F(exact.bf16_value(int(b))) for b in wb]
+    W_ = sum(x * x for x in xs) / len(xs) + F(float(np.float32(eps)))
+    return [exact.rnb_of_quotient(x * w, W_) for x, w in zip(xs, ws)]
+
+
+def _rand_bits(rng, n, lo=-8, hi=8):
+    v = rng.standard_normal(n) * 2.0 ** rng.uniform(lo, hi, n)
+    return np.array([bf(x) for x in v], np.uint16)
+
+
+@pytest.mark.parametrize("D", [2, 4, 8, 128])
+def test_rms_norm_head_matches_exact_brute_force(D):
+    rng = np.random.default_rng(D)
+    for trial in range(60 if D < 128 else 12):
+        x = _rand_bits(rng, D, -6, 6) if trial % 3 else _rand_bits(rng, D, -1, 1)
+        w = _rand_bits(rng, D, -2, 2)
+        if trial % 5 == 0:
+            x[:] = x[0]                            # constant vector
+        eps = [1e-6, 0.0, 1e-2][trial % 3]
+        if eps == 0.0 and not any(exact.bf16_value(int(b)) for b in x):
+            continue
+        got = [int(v) for v in oracle.rms_norm_head(x, w, eps)]
+        want = _exact_rms_head(x, w, eps)
+        # exact zeros: the oracle keeps the IEEE sign of x * w, the exact search returns +0
+        got = [0 if (g & 0x7FFF) == 0 else g for g in got]
+        want = [0 if (v & 0x7FFF) == 0 else v for v in want]
+        assert got == want, (D, trial)
+
+
+def test_rms_norm_head_closed_forms():
+    one = np.full(128, bf(1.0), np.uint16)
+    # constant vector a, weight 1, eps 0: every value is sign(a) exactly
+    for a in (3.0, -0.125, 1e-10, 6e4):
+        n = oracle.rms_norm_head(np.full(128, bf(a), np.uint16), one, 0.0)
+        assert (n == bf(math.copysign(1.0, a))).all()
+    # scale invariance with eps = 0 (a power-of-two rescale is exact in BF16)
+    rng = np.random.default_rng(5)
+    x = _rand_bits(rng, 128, -3, 3)
+    x2 = np.array([bf(exact.bf16_value(int(b)) * 2.0 ** 20) for b in x], np.uint16)
+    assert np.array_equal(oracle.rms_norm_head(x, one, 0.0), oracle.rms_norm_head(x2, one, 0.0))
+    # the weight multiplies: w = 2 doubles every value exactly
+    two = np.full(128, bf(2.0), np.uint16)
+    a = oracle.rms_norm_head(x, one, 1e-6)
+    b = oracle.rms_norm_head(x, two, 1e-6)
+    assert all(exact.bf16_value(int(v)) * 2 == exact.bf16_value(int(u)) for v, u in zip(a, b))
+    # eps dominates a tiny vector: n is x / sqrt(eps) to within one BF16 step
+    tiny = np.array([bf(1e-9)] * 128, np.uint16)
+    n = oracle.rms_norm_head(tiny, one, 1e-2)
+    approx = exact.bf16_value(int(tiny[0])) / math.sqrt(float(np.float32(1e-2)))
+    assert abs(exact.bf16_value(int(n[0])) - approx) <= approx * 2.0 ** -8
+
+
+def test_rms_norm_head_matches_torch_fp64_rms_norm():
+    rms_norm = getattr(torch.nn.functional, "rms_norm", None)
+    if rms_norm is None:
+        pytest.skip("torch without rms_norm")
+    rng = np.random.default_rng(9)
+    for _ in range(200):
+        x = _rand_bits(rng, 128, -4, 4)
+        w = _rand_bits(rng, 128, -1, 1)
+        xt = torch.tensor([exact.bf16_value(int(b)) for b in x], dtype=torch.float64)
+        wt = torch.tensor([exact.bf16_value(int(b)) for b in w], dtype=torch.float64)
+        ref = rms_norm(xt, (128,), wt, float(np.float32(1e-6))).numpy()
+        # fp64 -> BF16 with one rounding (torch's own cast goes through fp32)
+        ref = np.array([exact.nearest_bf16(F(float(v))) for v in ref], np.uint16)
+        assert np.array_equal(oracle.rms_norm_head(x, w, 1e-6), ref)
+
+
+def _torch_rope(nb, cs):
+    """Interleaved RoPE in eager fp32 torch ops (each op rounded separately)."""
+    n = torch.from_numpy(nb.view(np.int16)).view(torch.bfloat16).float()
+    c = torch.from_numpy(cs[:64].copy())
+    s = torch.from_numpy(cs[64:].copy())
+    a, b = n[0::2], n[1::2]
+    o = torch.empty(128, dtype=torch.float32)
+    o[0::2] = a * c - b * s
+    o[1::2] = b * c + a * s
+    return o.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_rope_matches_torch_eager_fp32_and_exact_steps():
+    rng = np.random.default_rng(21)
+    for trial in range(300):
+        nb = _rand_bits(rng, 128, -6, 6)
+        ang = rng.uniform(-1e4, 1e4, 64)
+        cs = np.concatenate([np.cos(ang), np.sin(ang)]).astype(np.float32)
+        got = oracle.rope_interleaved(nb, cs)
+        assert np.array_equal(got, _torch_rope(nb, cs)), trial
+        if trial < 20:
+            for i in range(64):
+                a, b = F(exact.bf16_value(int(nb[2 * i]))), F(exact.bf16_value(int(nb[2 * i + 1])))
+                c, s = F(float(cs[i])), F(float(cs[64 + i]))
+                r0 = F(exact.nearest_f32(a * c)) - F(exact.nearest_f32(b * s))
+                r1 = F(exact.nearest_f32(b * c)) + F(exact.nearest_f32(a * s))
+                for r, g in ((r0, got[2 * i]), (r1, got[2 * i + 1])):
+                    want = exact.nearest_bf16(F(exact.nearest_f32(r))) if r != 0 else 0
+                    assert (int(g) & 0x7FFF) == (want & 0x7FFF) and (r == 0 or int(g) == want)
+
+
+def test_rope_closed_forms():
+    rng = np.random.default_rng(22)
+    nb = _rand_bits(rng, 128, -6, 6)
+    ident = np.concatenate([np.ones(64), np.zeros(64)]).astype(np.float32)
+    assert np.array_equal(oracle.rope_interleaved(nb, ident), nb)
+    quarter = np.concatenate([np.zeros(64), np.ones(64)]).astype(np.float32)   # 90 degrees
+    o = oracle.rope_interleaved(nb, quarter)
+    assert np.array_equal(o[0::2], nb[1::2] ^ 0x8000) and np.array_equal(o[1::2], nb[0::2])
+    half = np.concatenate([-np.ones(64), np.zeros(64)]).astype(np.float32)     # 180 degrees
+    assert np.array_equal(oracle.rope_interleaved(nb, half) & 0x7FFF, nb & 0x7FFF)
+
+
+def test_qkv_epilogue_is_per_head_norm_rope_and_joint_text_first():
+    import workloads as W
+    d = W.qkv_inputs(3, 4, heads=2, seed=4, extra_cols=16)   # row stride > 3*heads*128
+    d["txt"]["eps"], d["img"]["eps"] = 1e-6, 1e-5
+    jq, jk, jv = oracle.qkv_epilogue(d["txt"], d["img"], heads=2)
+    assert jq.shape == (7, 2, 128)
+    for r in range(7):
+        st, rr = (d["txt"], r) if r < 3 else (d["img"], r - 3)
+        for h in range(2):
+            sl = slice(h * 128, h * 128 + 128)
+            for x, w, out in ((st["q"], st["wq"], jq), (st["k"], st["wk"], jk)):
+                n = oracle.rms_norm_head(x[rr, sl], w, st["eps"])
+                assert np.array_equal(out[r, h], oracle.rope_interleaved(n, st["cos_sin"][rr]))
+            assert np.array_equal(jv[r, h], st["v"][rr, sl])

@@ -44,6 +44,12 @@ CONFIGS = {
     # FP8 configuration's input_scale 0.1 stands for.
     "token_cat_nvfp4_flux": dict(op="token_cat_nvfp4", rows=4608, a_cols=6144, m_cols=18432,
                                  global_scale=60.0, seed=0),
+    # Attention-input epilogue after the packed QKV GEMM: 1024x1024 image -> 64x64 = 4096
+    # image tokens; text tokens 256 (Qwen-Image) / 512 (FLUX.2); head_dim 128.
+    "qkv_qwen": dict(op="qkv_epilogue", txt_tokens=256, img_tokens=4096, heads=24, eps=1e-6,
+                     seed=0),
+    "qkv_flux": dict(op="qkv_epilogue", txt_tokens=512, img_tokens=4096, heads=48, eps=1e-6,
+                     seed=1),
 }
 
 
@@ -101,10 +107,53 @@ def token_cat_inputs(rows: int, a_cols: int = 6144, m_cols: int = 18432, seed: i
     return dict(a=to_bf16_bits(a), m=to_bf16_bits(m))
 
 
+def rope_cache(positions: np.ndarray, head_dim: int = 128, theta: float = 10000.0) -> np.ndarray:
+    """fp32 [tokens, head_dim] cache rows (cos of the head_dim/2 pair angles, then sin).
+    positions: [tokens, head_dim/2] position index used by each pair."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    inv_freq = theta ** (-2.0 * i / head_dim)
+    ang = positions.astype(np.float64) * inv_freq[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def qkv_inputs(txt_tokens: int, img_tokens: int, heads: int, seed: int = 0, eps: float = 1e-6,
+               head_dim: int = 128, extra_cols: int = 0):
+    """Two streams of packed QKV GEMM output, [tokens, 3*heads*head_dim (+extra_cols)] BF16
+    (q | k | v side by side). q, k ~ N(0,1) times a per-channel gain exp(N(0, 0.5)) shared by
+    all heads (trained projections have uneven channels); v ~ N(0,1). RMSNorm weights ~
+    N(1, 0.3). cos/sin caches: text token t uses position t for every pair; image token
+    (y, x) of a square grid uses y for the first half of the pairs and x for the second."""
+    g = _gen(seed)
+    out = {}
+    side = int(round(img_tokens ** 0.5))
+    for name, n in (("txt", txt_tokens), ("img", img_tokens)):
+        width = 3 * heads * head_dim + extra_cols
+        gain = torch.exp(torch.randn(head_dim, generator=g) * 0.5)
+        qk = torch.randn(n, 2, heads, head_dim, generator=g) * gain
+        v = torch.randn(n, heads * head_dim, generator=g)
+        packed = torch.cat([qk.reshape(n, 2 * heads * head_dim), v,
+                            torch.randn(n, extra_cols, generator=g)], dim=1)
+        assert packed.shape[1] == width
+        bits = to_bf16_bits(packed)
+        hd = heads * head_dim
+        if name == "txt" or side * side != n:
+            pos = np.repeat(np.arange(n)[:, None], head_dim // 2, axis=1)
+        else:
+            yy, xx = np.divmod(np.arange(n), side)
+            pos = np.concatenate([np.repeat(yy[:, None], head_dim // 4, axis=1),
+                                  np.repeat(xx[:, None], head_dim // 4, axis=1)], axis=1)
+        out[name] = dict(packed=bits, q=bits[:, :hd], k=bits[:, hd:2 * hd], v=bits[:, 2 * hd:3 * hd],
+                         ld=width,
+                         wq=to_bf16_bits(1.0 + 0.3 * torch.randn(head_dim, generator=g)),
+                         wk=to_bf16_bits(1.0 + 0.3 * torch.randn(head_dim, generator=g)),
+                         cos_sin=rope_cache(pos, head_dim), eps=eps)
+    return out
+
+
 def config_inputs(name: str, rows: int | None = None, seed: int | None = None):
     """Inputs of a named configuration (optionally with fewer rows / another seed)."""
     c = CONFIGS[name]
-    r = c["rows"] if rows is None else rows
+    r = c.get("rows") if rows is None else rows
     s = c["seed"] if seed is None else seed
     if c["op"] == "nss_fp8":
         n_mod = c.get("n_samples", 1)
@@ -115,4 +164,6 @@ def config_inputs(name: str, rows: int | None = None, seed: int | None = None):
         return residual_inputs(r, c["cols"], seed=s)
     if c["op"] in ("token_cat_fp8", "token_cat_nvfp4"):
         return token_cat_inputs(r, c["a_cols"], c["m_cols"], seed=s)
+    if c["op"] == "qkv_epilogue":
+        return qkv_inputs(c["txt_tokens"], c["img_tokens"], c["heads"], seed=s, eps=c["eps"])
     raise KeyError(name)
