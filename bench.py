@@ -330,9 +330,48 @@ def extra_cases(torch, lib, l2, only=None):
         case.keep = (bufs, s)
         return case
 
+    def qkv_qwen():
+        import fp8_quant_row_gb300._capi as capi
+        c = W.CONFIGS["qkv_qwen"]
+        d = W.config_inputs("qkv_qwen")
+        H = c["heads"]
+        T = c["txt_tokens"] + c["img_tokens"]
+        per = T * (3 * H * 128 * 2 * 2 + 128 * 4)
+        n = n_sets_for(per, l2)
+        sets = []
+        for _ in range(n):
+            streams, keep = [], []
+            for key in ("txt", "img"):
+                st = d[key]
+                packed = dev_bf16(torch, st["packed"])
+                wq, wk = dev_bf16(torch, st["wq"]), dev_bf16(torch, st["wk"])
+                cs = torch.from_numpy(st["cos_sin"]).cuda()
+                hd = H * 128
+                streams.append(capi.QkvStream(packed.data_ptr(), packed.data_ptr() + hd * 2,
+                                              packed.data_ptr() + 2 * hd * 2, packed.shape[1],
+                                              packed.shape[0], wq.data_ptr(), wk.data_ptr(),
+                                              cs.data_ptr(), st["eps"]))
+                keep += [packed, wq, wk, cs]
+            outs = [torch.empty(T, H, 128, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+            sets.append((streams, outs, keep))
+
+        def qkv(i):
+            streams, outs, _ = sets[i % len(sets)]
+            st = lib.fp8q_qkv_epilogue(outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(),
+                                       streams[0], streams[1], H, sh_())
+            if st:
+                raise RuntimeError(f"qkv_epilogue status {st}")
+
+        case = Case("qkv_epilogue", qkv, n, per, T, "qkv_epilogue_qwen",
+                    f"packed QKV bf16 text [{c['txt_tokens']},{3 * H * 128}] + image "
+                    f"[{c['img_tokens']},{3 * H * 128}], {H} heads x 128 -> joint q, k, v "
+                    f"[{T},{H},128] (RMSNorm + interleaved RoPE on q, k)")
+        case.keep = sets
+        return case
+
     builders = {"scale_residual_qwen": scale_residual_qwen, "bias_mul_add_qwen": bias_mul_add_qwen,
                 "nss_flux": nss_flux, "token_cat_flux": token_cat_flux,
-                "token_cat_nvfp4_flux": token_cat_nvfp4_flux}
+                "token_cat_nvfp4_flux": token_cat_nvfp4_flux, "qkv_qwen": qkv_qwen}
     return {k: f for k, f in builders.items() if only is None or k == only}
 
 
@@ -616,7 +655,7 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile-only", choices=("nss_qwen", "scale_residual_qwen",
-                                               "token_cat_nvfp4_flux",
+                                               "token_cat_nvfp4_flux", "qkv_qwen",
                                                "bias_mul_add_qwen", "nss_flux", "token_cat_flux"),
                     help="only launch this workload (W+K launches, no timing): for ncu captures")
     args = ap.parse_args()

@@ -10,6 +10,7 @@ library's sm_103a kernels; there is no CPU or eager fallback.
     y = bias_mul_add(x, bias, gate, residual)
     q = token_cat_fp8(attention, mlp, input_scale)
     q4, sf = token_cat_nvfp4(attention, mlp, global_scale)            # uint8 codes / scales
+    jq, jk, jv = qkv_epilogue(txt, img, heads)      # per-head QK RMSNorm + RoPE, joint pack
 """
 from __future__ import annotations
 
@@ -20,7 +21,7 @@ from ._build import build
 from ._capi import Fp8qError
 
 __all__ = ["nss_fp8", "scale_residual_nss_fp8", "bias_mul_add", "token_cat_fp8",
-           "token_cat_nvfp4", "nvfp4_scale_bytes", "build",
+           "token_cat_nvfp4", "nvfp4_scale_bytes", "qkv_epilogue", "build",
            "Fp8qError", "library_path"]
 
 EPS = 1e-6
@@ -153,3 +154,51 @@ def token_cat_nvfp4(a, m, global_scale, *, q=None, sf=None, stream=None):
                                           _stream_handle(stream))
     _capi.check(st, "fp8q_token_cat_nvfp4")
     return q, sf
+
+
+HEAD_DIM = 128
+
+
+def _qkv_stream(st: dict, heads: int) -> "_capi.QkvStream":
+    q, k, v = st["q"], st["k"], st["v"]
+    tokens = q.shape[0]
+    if tokens == 0:  # an empty stream: nothing is read from it
+        return _capi.QkvStream(None, None, None, heads * HEAD_DIM, 0, None, None, None,
+                               float(st.get("eps", EPS)))
+    for name in ("q", "k", "v"):
+        t = st[name]
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
+            raise TypeError(f"{name}: expected a 2-D CUDA bfloat16 tensor with unit column stride")
+        if t.shape[0] != tokens or t.shape[1] < heads * HEAD_DIM or t.stride(0) != q.stride(0):
+            raise TypeError(f"{name}: rows, width or row stride differ from q")
+    for name in ("q_weight", "k_weight"):
+        _bf16(st[name], name)
+        if st[name].numel() != HEAD_DIM:
+            raise TypeError(f"{name}: expected {HEAD_DIM} values")
+    cs = st["cos_sin"]
+    if cs.dtype != torch.float32 or not cs.is_cuda or not cs.is_contiguous() or \
+            tuple(cs.shape) != (tokens, HEAD_DIM):
+        raise TypeError(f"cos_sin: expected a contiguous CUDA float32 [{tokens}, {HEAD_DIM}]")
+    return _capi.QkvStream(q.data_ptr(), k.data_ptr(), v.data_ptr(), q.stride(0), tokens,
+                           st["q_weight"].data_ptr(), st["k_weight"].data_ptr(), cs.data_ptr(),
+                           float(st.get("eps", EPS)))
+
+
+def qkv_epilogue(txt: dict, img: dict, heads: int, *, out=None, stream=None):
+    """Attention inputs after the packed QKV GEMM: returns joint (q, k, v), each bfloat16
+    [txt_tokens + img_tokens, heads, 128], text first. Per head of q and k: RMSNorm with the
+    stream's weight and eps, then interleaved RoPE with the stream's fp32 cos/sin cache; v is
+    copied. `txt` / `img`: dicts with q, k, v (2-D views of the GEMM output, e.g. column
+    slices of one [tokens, 3*heads*128] tensor), q_weight, k_weight, cos_sin and eps."""
+    ts, ims = _qkv_stream(txt, heads), _qkv_stream(img, heads)
+    total = ts.tokens + ims.tokens
+    like = txt["q"]
+    if out is None:
+        out = tuple(torch.empty(total, heads, HEAD_DIM, dtype=torch.bfloat16, device=like.device)
+                    for _ in range(3))
+    for t in out:
+        _out(t, (total, heads, HEAD_DIM), torch.bfloat16, like, "out")
+    st = _capi.lib().fp8q_qkv_epilogue(out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
+                                       ts, ims, heads, _stream_handle(stream))
+    _capi.check(st, "fp8q_qkv_epilogue")
+    return out

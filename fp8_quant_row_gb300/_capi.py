@@ -20,8 +20,17 @@ STATUS = {0: "FP8Q_OK", 1: "FP8Q_ERR_NULL", 2: "FP8Q_ERR_ALIGN", 3: "FP8Q_ERR_SH
 #: every function include/fp8q.h declares
 SYMBOLS = ("fp8q_nss_fp8", "fp8q_scale_residual_nss_fp8", "fp8q_bias_mul_add",
            "fp8q_token_cat_fp8", "fp8q_token_cat_nvfp4", "fp8q_nvfp4_scale_bytes",
+           "fp8q_qkv_epilogue",
            "fp8q_status_string", "fp8q_last_cuda_error",
            "fp8q_last_error_detail", "fp8q_version")
+
+
+class QkvStream(ctypes.Structure):
+    """struct fp8q_qkv_stream of include/fp8q.h."""
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("ld", ctypes.c_int64), ("tokens", ctypes.c_int64),
+                ("q_weight", ctypes.c_void_p), ("k_weight", ctypes.c_void_p),
+                ("cos_sin", ctypes.c_void_p), ("eps", ctypes.c_float)]
 
 
 class Fp8qError(RuntimeError):
@@ -51,10 +60,12 @@ def lib():
         L.fp8q_bias_mul_add.argtypes = [vp, vp, vp, vp, vp, i64, i64, vp]
         L.fp8q_token_cat_fp8.argtypes = [vp, vp, i64, vp, i64, vp, i64, vp]
         L.fp8q_token_cat_nvfp4.argtypes = [vp, vp, vp, i64, vp, i64, vp, i64, vp]
+        L.fp8q_qkv_epilogue.argtypes = [vp, vp, vp, ctypes.POINTER(QkvStream),
+                                         ctypes.POINTER(QkvStream), i64, vp]
         L.fp8q_nvfp4_scale_bytes.argtypes = [i64, i64]
         L.fp8q_nvfp4_scale_bytes.restype = i64
         for name in ("fp8q_nss_fp8", "fp8q_scale_residual_nss_fp8", "fp8q_bias_mul_add",
-                     "fp8q_token_cat_fp8", "fp8q_token_cat_nvfp4"):
+                     "fp8q_token_cat_fp8", "fp8q_token_cat_nvfp4", "fp8q_qkv_epilogue"):
             getattr(L, name).restype = i32
         L.fp8q_status_string.argtypes = [i32]
         L.fp8q_status_string.restype = ctypes.c_char_p

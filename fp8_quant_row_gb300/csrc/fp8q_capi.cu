@@ -17,6 +17,7 @@
 #include "elementwise_kernels.cuh"
 #include "nss_kernels.cuh"
 #include "nvfp4_kernels.cuh"
+#include "qkv_kernels.cuh"
 
 namespace {
 
@@ -99,6 +100,11 @@ fp8q_status blocks_per_sm(const void* fn, int threads, size_t smem, int* blocks)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+// Bytes spanned by `tokens` rows of `width` BF16 values at a stride of `ld` values.
+size_t strided_bytes(int64_t tokens, int64_t ld, int64_t width) {
+  return tokens > 0 ? size_t((tokens - 1) * ld + width) * 2 : 0;
+}
 
 struct Range {
   const void* p;
@@ -411,6 +417,74 @@ fp8q_status fp8q_token_cat_nvfp4(uint8_t* q_fp4, uint8_t* sf_e4m3, const void* a
                 q_fp4, sf_e4m3, static_cast<const uint16_t*>(a_bf16), int(a_cols / 64),
                 static_cast<const uint16_t*>(m_bf16), int(m_cols / 64), global_scale, rows,
                 rows_pad);
+}
+
+fp8q_status fp8q_qkv_epilogue(void* joint_q, void* joint_k, void* joint_v,
+                              const fp8q_qkv_stream* txt, const fp8q_qkv_stream* img,
+                              int64_t heads, cudaStream_t stream) {
+  if (!txt || !img) return FP8Q_ERR_NULL;
+  if (heads < 1 || heads > 4096) return FP8Q_ERR_SHAPE;
+  const int64_t width = heads * fp8q::kHeadDim;
+  const fp8q_qkv_stream* st[2] = {txt, img};
+  for (const fp8q_qkv_stream* s : st) {
+    if (s->tokens < 0 || (s->tokens > 0 && (s->ld < width || s->ld % 16 != 0)))
+      return FP8Q_ERR_SHAPE;
+  }
+  const int64_t total = txt->tokens + img->tokens;
+  if (total == 0) return FP8Q_OK;
+  for (const fp8q_qkv_stream* s : st) {
+    if (s->tokens == 0) continue;
+    if (!(s->eps > 0.0f) || !std::isfinite(s->eps)) return FP8Q_ERR_VALUE;
+  }
+  if (!joint_q || !joint_k || !joint_v) return FP8Q_ERR_NULL;
+  for (const fp8q_qkv_stream* s : st) {
+    if (s->tokens == 0) continue;
+    if (!s->q || !s->k || !s->v || !s->q_weight || !s->k_weight || !s->cos_sin)
+      return FP8Q_ERR_NULL;
+    if (!aligned32(s->q) || !aligned32(s->k) || !aligned32(s->v) || !aligned32(s->q_weight) ||
+        !aligned32(s->k_weight) || !aligned32(s->cos_sin))
+      return FP8Q_ERR_ALIGN;
+  }
+  if (!aligned32(joint_q) || !aligned32(joint_k) || !aligned32(joint_v)) return FP8Q_ERR_ALIGN;
+  const size_t out_bytes = size_t(total) * size_t(width) * 2;
+  const Range outs[3] = {{joint_q, out_bytes}, {joint_k, out_bytes}, {joint_v, out_bytes}};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(outs[i], outs[j])) return FP8Q_ERR_ALIAS;
+    for (const fp8q_qkv_stream* s : st) {
+      if (s->tokens == 0) continue;
+      const Range ins[6] = {{s->q, strided_bytes(s->tokens, s->ld, width)},
+                            {s->k, strided_bytes(s->tokens, s->ld, width)},
+                            {s->v, strided_bytes(s->tokens, s->ld, width)},
+                            {s->q_weight, size_t(fp8q::kHeadDim) * 2},
+                            {s->k_weight, size_t(fp8q::kHeadDim) * 2},
+                            {s->cos_sin, size_t(s->tokens) * fp8q::kHeadDim * 4}};
+      for (const Range& r : ins)
+        if (overlap(outs[i], r)) return FP8Q_ERR_ALIAS;
+    }
+  }
+  const DeviceInfo* dev = nullptr;
+  fp8q_status stt = current_device(&dev);
+  if (stt != FP8Q_OK) return stt;
+  fp8q::QkvParams p;
+  p.jq = static_cast<uint16_t*>(joint_q);
+  p.jk = static_cast<uint16_t*>(joint_k);
+  p.jv = static_cast<uint16_t*>(joint_v);
+  fp8q::QkvStream* dstp[2] = {&p.txt, &p.img};
+  for (int i = 0; i < 2; ++i) {
+    dstp[i]->q = static_cast<const uint16_t*>(st[i]->q);
+    dstp[i]->k = static_cast<const uint16_t*>(st[i]->k);
+    dstp[i]->v = static_cast<const uint16_t*>(st[i]->v);
+    dstp[i]->wq = static_cast<const uint16_t*>(st[i]->q_weight);
+    dstp[i]->wk = static_cast<const uint16_t*>(st[i]->k_weight);
+    dstp[i]->cos_sin = st[i]->cos_sin;
+    dstp[i]->ld = st[i]->ld;
+    dstp[i]->tokens = st[i]->tokens;
+    dstp[i]->eps = st[i]->eps;
+  }
+  p.heads = int(heads);
+  const unsigned gx = unsigned(total < 0x7FFFFFFF ? total : 0x7FFFFFFF);
+  return launch(fp8q::qkv_epilogue_kernel, dim3(gx), dim3(fp8q::kQkvWarps * 32), 0, stream, p);
 }
 
 const char* fp8q_status_string(int status) {

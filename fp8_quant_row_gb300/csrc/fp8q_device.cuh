@@ -245,6 +245,9 @@ namespace fp8q {
 // packed fp32 pairs (sm_100+ f32x2 instructions: one issue slot for two lanes of work)
 // ------------------------------------------------------------------------------------------
 
+// ptxas may fuse a mul.rn.f32x2 whose result feeds an add.rn.f32x2 into one fused
+// multiply-add (observed on sm_103a, unlike the scalar _rn intrinsics): where a product must
+// be rounded on its own before a sum, use __fmul_rn / __fadd_rn instead.
 struct f2 {
   unsigned long long v;
 };

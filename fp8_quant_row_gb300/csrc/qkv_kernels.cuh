@@ -1,0 +1,238 @@
+// qkv_kernels.cuh -- attention-input epilogue after the packed QKV GEMM, for sm_103a.
+//
+// "sglang #37123 - Qwen-Image FP8 QKV fusion" (implementation breakdown item 3, key source
+// snippets) and "sglang #37162 - FLUX.2 FP8 LayerNorm/quant/QKV fusions" (implementation
+// breakdown item 3): per token of two streams (text, image) and per head of 128 values,
+//   Q, K:  n_j = RN_bf16(x_j * w_j / sqrt(mean(x^2) + eps))         (exact value, one rounding)
+//          o[2i]   = RN_bf16(RN(RN(n[2i] c_i) - RN(n[2i+1] s_i)))  (interleaved RoPE, fp32
+//          o[2i+1] = RN_bf16(RN(RN(n[2i+1] c_i) + RN(n[2i] s_i)))   products and sum)
+//   V:     copied,
+// written to joint [text tokens + image tokens, heads, 128] buffers, text first.
+//
+// Layout: one CTA per joint token (grid-stride), 6 warps: two per kind (Q, K, V). A warp takes
+// four heads at a time; 8 lanes per head, 16 consecutive values (one 32-byte load) per lane,
+// so each lane's 8 packed BF16 words are exactly its 8 RoPE pairs. A Q/K warp loads all its
+// heads of the token before computing any.
+//
+// Exactness of n: sum(x^2) per head is formed without rounding error that matters. Squares
+// of BF16 values are exact in fp32. They are accumulated from an offset K2 = 2^(2E+9) >= 128
+// max x^2 (E the exponent of the head's max |x|), so every partial sum lies in [K2, 2 K2)
+// with one fixed ulp u: s = fma(v, v, S) and e = fma(v, v, S - s) give the exact rounding
+// error; the e are added to a second offset accumulator 48u (one binade, ulp u 2^-18) with
+// the FastTwoSum error kept, and those second-level errors summed in fp32 (their rounding is
+// ~2^-53 of the total). Accumulator offsets come off as exact integers of their ulps, which
+// the 8 lanes of a head add as integers. 1/sqrt(mean + eps) is a double-float (~2^-45). The
+// fast path t = fma(p, r_hi, p r_lo), p = x w (exact), is within one fp32 ulp of the exact
+// value; only values whose low 16 bits lie within 8 of the BF16 midpoint pattern take the
+// exact path (TwoProduct + the tie broken by the low part).
+#pragma once
+
+#include "fp8q_device.cuh"
+
+namespace fp8q {
+
+constexpr int kQkvWarps = 6;       // per CTA: 2 x (Q, K, V)
+constexpr int kQkvBatch = 3;       // heads-of-four loaded ahead per Q/K warp
+constexpr int kHeadDim = 128;
+
+struct QkvStream {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  const uint16_t* wq;       // [128] RMSNorm weight of Q
+  const uint16_t* wk;       // [128] RMSNorm weight of K
+  const float* cos_sin;     // [tokens, 128]: cos of pair i at i, sin at 64 + i
+  int64_t ld;               // row stride of q, k, v in elements
+  int64_t tokens;
+  float eps;
+};
+
+struct QkvParams {
+  uint16_t* jq;
+  uint16_t* jk;
+  uint16_t* jv;
+  QkvStream txt, img;
+  int heads;
+};
+
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float(uint32_t(e + 127) << 23); }
+
+__device__ __forceinline__ void ld_nc32(const void* p, uint32_t (&w)[8]) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+}
+
+// Integer-valued float c (|c| < 2^31) times the power of two `scale`, as a double-float.
+__device__ __forceinline__ dd int_to_dd(int c, float scale) {
+  const float hi = __int2float_rn(c);
+  const float lo = __int2float_rn(c - __float2int_rz(hi));
+  return dd{__fmul_rn(hi, scale), __fmul_rn(lo, scale)};
+}
+
+// 1 / sqrt(sum(x^2) / 128 + eps) for the head held by this lane's group of 8 lanes.
+__device__ __forceinline__ dd head_rrms(const uint32_t (&w)[8], float eps) {
+  uint32_t m = max_u16x2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu);
+#pragma unroll
+  for (int i = 2; i < 8; ++i) m = max_u16x2(m, w[i] & 0x7FFF7FFFu);
+  uint32_t mx = max(m & 0xFFFFu, m >> 16);
+  mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+  mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+  mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+  const int E = min(max(int(mx >> 7) - 127, -40), 56);
+  const float K2 = exp2i(2 * E + 9);
+  const float K3 = 1.5f * exp2i(2 * E - 9);  // 48 u, u = 2^(2E - 14)
+  f2 S = f2_make(K2, K2), R = f2_make(K3, K3), T = f2_make(0.0f, 0.0f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const f2 v = bf2_to_f2(w[i]);
+    const f2 s = fma2(v, v, S);
+    const f2 e = fma2(v, v, sub2(S, s));   // exact error of s
+    S = s;
+    const f2 r = add2(R, e);
+    T = add2(T, sub2(e, sub2(r, R)));      // FastTwoSum error (|R| > |e|)
+    R = r;
+  }
+  const float inv_u = exp2i(14 - 2 * E);
+  int cs = __float2int_rn(__fmul_rn(__fsub_rn(f2_lo(S), K2), inv_u)) +
+           __float2int_rn(__fmul_rn(__fsub_rn(f2_hi(S), K2), inv_u));
+  const float inv_u2 = exp2i(32 - 2 * E);   // 1 / (u 2^-18)
+  int cr = __float2int_rn(__fmul_rn(__fsub_rn(f2_lo(R), K3), inv_u2)) +
+           __float2int_rn(__fmul_rn(__fsub_rn(f2_hi(R), K3), inv_u2));
+  float t = __fadd_rn(f2_lo(T), f2_hi(T));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    cs += __shfl_xor_sync(0xFFFFFFFFu, cs, o);
+    cr += __shfl_xor_sync(0xFFFFFFFFu, cr, o);
+    t = __fadd_rn(t, __shfl_xor_sync(0xFFFFFFFFu, t, o));
+  }
+  dd sum = dd_add(int_to_dd(cs, exp2i(2 * E - 14)), int_to_dd(cr, exp2i(2 * E - 32)));
+  sum = dd_add(sum, dd{t, 0.0f});
+  const dd ms = dd{__fmul_rn(sum.hi, 1.0f / kHeadDim), __fmul_rn(sum.lo, 1.0f / kHeadDim)};
+  return dd_rsqrt(dd_add(ms, dd{eps, 0.0f}));
+}
+
+// Exact path: RN_bf16(p * (r_hi + r_lo)) for an exact fp32 product p = x w.
+__device__ __noinline__ uint32_t scaled_exact_bits(float p, float r_hi, float r_lo) {
+  float ph, pe;
+  two_prod(p, r_hi, ph, pe);
+  pe = __fmaf_rn(p, r_lo, pe);
+  float t_hi, t_lo;
+  fast_two_sum(ph, pe, t_hi, t_lo);
+  const uint32_t u = __float_as_uint(t_hi);
+  if ((u & 0xFFFFu) == 0x8000u && t_lo != 0.0f) {
+    const bool mag_up = (t_lo > 0.0f) == (t_hi > 0.0f);
+    return (u >> 16) + (mag_up ? 1u : 0u);
+  }
+  return pack_bf16x2(t_hi, 0.0f) & 0xFFFFu;
+}
+
+// RMSNorm + RoPE of this lane's 16 values (8 pairs); x, wt: packed BF16 words; c, s: the
+// lane's 8 cos and 8 sin values. Returns the 8 output words.
+__device__ __forceinline__ void qk_lane(const uint32_t (&x)[8], const uint32_t (&wt)[8],
+                                        const float (&c)[8], const float (&s)[8], dd r,
+                                        uint32_t (&o)[8]) {
+  const f2 rh = f2_make(r.hi, r.hi), rl = f2_make(r.lo, r.lo);
+  uint32_t n[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const f2 p = mul2(bf2_to_f2(x[i]), bf2_to_f2(wt[i]));   // exact
+    const f2 t = fma2(p, rh, mul2(p, rl));
+    n[i] = pack_bf16x2(f2_lo(t), f2_hi(t));
+    if (near_bf16_midpoint(f2_lo(t)))   // rare (~2^-11): out-of-line exact rounding
+      n[i] = (n[i] & 0xFFFF0000u) | scaled_exact_bits(f2_lo(p), r.hi, r.lo);
+    if (near_bf16_midpoint(f2_hi(t)))
+      n[i] = (n[i] & 0xFFFFu) | (scaled_exact_bits(f2_hi(p), r.hi, r.lo) << 16);
+  }
+  // Scalar _rn intrinsics: the products must be rounded before the sum (a packed
+  // mul.rn.f32x2 feeding add.rn.f32x2 was fused into one rounding on sm_103a).
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a = bf_lo(n[i]), b = bf_hi(n[i]);        // (n[2i], n[2i+1])
+    const float o0 = __fsub_rn(__fmul_rn(a, c[i]), __fmul_rn(b, s[i]));
+    const float o1 = __fadd_rn(__fmul_rn(b, c[i]), __fmul_rn(a, s[i]));
+    o[i] = pack_bf16x2(o0, o1);
+  }
+}
+
+__global__ void __launch_bounds__(kQkvWarps * 32) qkv_epilogue_kernel(QkvParams P) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kind = warp >> 1;       // 0: Q, 1: K, 2: V
+  const int first_quad = warp & 1;  // the two warps of a kind take alternate heads-of-four
+  const int g = lane >> 3;          // head within a heads-of-four
+  const int u = lane & 7;           // 16-value slice of the head
+  const int heads = P.heads;
+  const int quads = (heads + 3) >> 2;
+  const int64_t row_len = int64_t(heads) * kHeadDim;
+  const int64_t total = P.txt.tokens + P.img.tokens;
+  wait_for_producers();
+
+  for (int64_t jt = blockIdx.x; jt < total; jt += gridDim.x) {
+    const bool is_txt = jt < P.txt.tokens;
+    // field-wise selects keep the parameters in registers (a reference to either stream
+    // would force a local copy of both)
+    auto sel = [is_txt](auto a, auto b) { return is_txt ? a : b; };
+    const int64_t row = is_txt ? jt : jt - P.txt.tokens;
+    const int64_t ld = sel(P.txt.ld, P.img.ld);
+    const uint16_t* base = kind == 0 ? sel(P.txt.q, P.img.q)
+                         : kind == 1 ? sel(P.txt.k, P.img.k) : sel(P.txt.v, P.img.v);
+    const uint16_t* src = base + row * ld + u * 16;
+    uint16_t* dst = (kind == 0 ? P.jq : kind == 1 ? P.jk : P.jv) + jt * row_len + u * 16;
+    if (kind == 2) {
+      for (int qd0 = first_quad; qd0 < quads; qd0 += 2 * kQkvBatch) {
+        uint32_t w[kQkvBatch][8];
+#pragma unroll
+        for (int b = 0; b < kQkvBatch; ++b) {
+          const int h = (qd0 + 2 * b) * 4 + g;
+          if (qd0 + 2 * b < quads && h < heads) ld_stream32(src + h * kHeadDim, w[b]);
+        }
+#pragma unroll
+        for (int b = 0; b < kQkvBatch; ++b) {
+          const int h = (qd0 + 2 * b) * 4 + g;
+          if (qd0 + 2 * b < quads && h < heads) st_stream32(dst + h * kHeadDim, w[b]);
+        }
+      }
+      continue;
+    }
+    const float eps = sel(P.txt.eps, P.img.eps);
+    uint32_t wt[8];
+    ld_nc32((kind == 0 ? sel(P.txt.wq, P.img.wq) : sel(P.txt.wk, P.img.wk)) + u * 16, wt);
+    float c[8], s[8];
+    {
+      uint32_t cw[8], sw[8];
+      const float* cs = sel(P.txt.cos_sin, P.img.cos_sin) + row * kHeadDim + u * 8;
+      ld_nc32(cs, cw);
+      ld_nc32(cs + 64, sw);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = __uint_as_float(cw[i]);
+        s[i] = __uint_as_float(sw[i]);
+      }
+    }
+    for (int qd0 = first_quad; qd0 < quads; qd0 += 2 * kQkvBatch) {
+      uint32_t x[kQkvBatch][8];
+#pragma unroll
+      for (int b = 0; b < kQkvBatch; ++b) {
+        const int h = (qd0 + 2 * b) * 4 + g;
+        if (qd0 + 2 * b < quads && h < heads) {
+          ld_stream32(src + h * kHeadDim, x[b]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[b][i] = 0u;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kQkvBatch; ++b) {
+        if (qd0 + 2 * b >= quads) break;  // warp-uniform
+        const dd r = head_rrms(x[b], eps);
+        uint32_t o[8];
+        qk_lane(x[b], wt, c, s, r, o);
+        const int h = (qd0 + 2 * b) * 4 + g;
+        if (h < heads) st_stream32(dst + h * kHeadDim, o);
+      }
+    }
+  }
+}
+
+}  // namespace fp8q

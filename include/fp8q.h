@@ -8,6 +8,8 @@
  *   token_cat_fp8           E4M3 quantisation of the row concat [a | m] without a BF16 concat.
  *   token_cat_nvfp4         NVFP4 quantisation (E2M1 codes + 128x4-tiled E4M3 block scales)
  *                           of the same row concat.
+ *   qkv_epilogue            after the packed QKV GEMM: per-head Q/K RMSNorm + interleaved RoPE,
+ *                           V copy, joint [text, image] attention inputs.
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers to row-major, contiguous arrays on the current
@@ -40,6 +42,12 @@
  *               (attention 6144 + MLP 18432 -> NVFP4 without the concat), implementation
  *               breakdown items 1-3 (per-group conversion, 128x4-swizzled scale offsets,
  *               input_scale_inv as the global scale, 32-byte aligned dense BF16 inputs).
+ *   [QWEN-QKV]  "sglang #37123 - Qwen-Image FP8 QKV fusion": implementation breakdown item 3
+ *               (Q/K RMSNorm + RoPE, V copy, joint [text, image] output, head_dim 128, 32-byte
+ *               aligned strided views of the packed GEMM output), key source snippets
+ *               (per-stream norm weights, epsilons and cos/sin caches; is_neox=False).
+ *   [FLUX-QKV]  "sglang #37162 - FLUX.2 FP8 LayerNorm/quant/QKV fusions": implementation
+ *               breakdown item 3 (QK RMSNorm, RoPE, QKV pack, text/image concat).
  *   [NVFP4]     the public NVFP4 format: E2M1 elements, one E4M3 scale per 16 consecutive
  *               elements of a row, an fp32 per-tensor scale; 128x4 scale tiles of FP4 GEMMs.
  */
@@ -180,6 +188,41 @@ fp8q_status fp8q_token_cat_nvfp4(uint8_t* q_fp4, uint8_t* sf_e4m3, const void* a
  * ceil(rows/128)*128 * ceil(cols/64)*4. -1 for rows < 0 or cols not a positive multiple of 16.
  * Host-only arithmetic. */
 int64_t fp8q_nvfp4_scale_bytes(int64_t rows, int64_t cols);
+
+/* One input stream of fp8q_qkv_epilogue (all pointers device pointers, 32-byte aligned). */
+typedef struct fp8q_qkv_stream {
+    const void* q;         /* [tokens, ld] bf16; head h at values h*128 .. h*128+127        */
+    const void* k;         /* same layout (the packed GEMM output: q, k, v side by side)    */
+    const void* v;
+    int64_t ld;            /* row stride in values: >= heads*128, a multiple of 16           */
+    int64_t tokens;        /* rows of this stream (0 allowed: nothing read)                  */
+    const void* q_weight;  /* [128] bf16 RMSNorm weight of Q                                 */
+    const void* k_weight;  /* [128] bf16 RMSNorm weight of K                                 */
+    const float* cos_sin;  /* [tokens, 128] fp32 RoPE cache: cos of pair i at i, sin at 64+i  */
+    float eps;             /* RMSNorm epsilon, finite and > 0 (FP8Q_ERR_VALUE otherwise)     */
+} fp8q_qkv_stream;
+
+/*
+ * Attention-input epilogue after the packed QKV GEMM [QWEN-QKV; FLUX-QKV], head_dim 128.
+ * Joint row r < txt->tokens comes from text row r, the others from image row r - txt->tokens.
+ * For every head h of a row (x = that head's 128 values of q or k, w the stream's weight):
+ *   n_j    = RN_bf16(x_j * w_j / sqrt(sum_i x_i^2 / 128 + eps))        one rounding of the
+ *                                                                       exact value
+ *   o[2i]   = RN_bf16(RN32(RN32(n[2i] c_i) - RN32(n[2i+1] s_i)))        interleaved RoPE with
+ *   o[2i+1] = RN_bf16(RN32(RN32(n[2i+1] c_i) + RN32(n[2i] s_i)))        c_i = cos_sin[row][i],
+ *                                                                       s_i = cos_sin[row][64+i]
+ *   joint_q[r, h, :] = o(q),  joint_k[r, h, :] = o(k),  joint_v[r, h, :] = v (bit copy)
+ *
+ *   joint_q, joint_k, joint_v  out  [txt->tokens + img->tokens, heads, 128] bf16, contiguous,
+ *                                   32-byte aligned
+ *   heads       1 .. 4096
+ *   Aliasing: the three outputs are disjoint from each other and from every input.
+ *   Values must be finite with |x| < 2^56; a head whose values are all below 2^-40 is
+ *   normalised with eps dominating (its squares are not summed exactly).
+ */
+fp8q_status fp8q_qkv_epilogue(void* joint_q, void* joint_k, void* joint_v,
+                              const fp8q_qkv_stream* txt, const fp8q_qkv_stream* img,
+                              int64_t heads, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string; never NULL). */
 const char* fp8q_status_string(int status);

@@ -13,7 +13,8 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: long-running CPU test")
 
 
-# Mismatch counts of the LayerNorm parity checks (y elements that differ from the oracle by
+# Mismatch counts of the one-ulp parity checks (LayerNorm y, QKV-epilogue q and k: elements
+# that differ from the oracle by
 # one bf16 ulp), reported at the end of the run.
 PARITY_COUNTS = []
 
@@ -24,7 +25,7 @@ def pytest_terminal_summary(terminalreporter):
     total = sum(n for _, n, _ in PARITY_COUNTS)
     elems = sum(e for _, _, e in PARITY_COUNTS)
     terminalreporter.write_line(
-        f"LayerNorm parity: {len(PARITY_COUNTS)} checks, {elems} y elements, "
+        f"one-ulp parity (LayerNorm y, QKV q/k): {len(PARITY_COUNTS)} checks, {elems} elements, "
         f"{total} differ from the oracle by 1 bf16 ulp (none by more)")
     for what, n, e in PARITY_COUNTS:
         if n:

@@ -183,3 +183,30 @@ def test_nvfp4_scale_bytes(L):
     assert f(129, 80) == 256 * 8
     assert f(0, 64) == 0
     assert f(-1, 64) == -1 and f(4, 24) == -1 and f(4, 0) == -1
+
+
+def test_qkv_epilogue_argument_checks(L):
+    import fp8_quant_row_gb300._capi as capi
+
+    def stream(base, tokens=4, ld=3 * 24 * 128, eps=1e-6):
+        return capi.QkvStream(base, base + 24 * 256, base + 48 * 256, ld, tokens,
+                              base + 100 * A, base + 100 * A + 4096, base + 101 * A, eps)
+
+    def call(jq=A, jk=2 * A, jv=3 * A, txt=None, img=None, heads=24):
+        txt = txt or stream(10 * A)
+        img = img or stream(20 * A)
+        return L.fp8q_qkv_epilogue(jq, jk, jv, txt, img, heads, None)
+
+    assert call(heads=0) == SHAPE
+    assert call(txt=stream(10 * A, ld=24 * 128 - 16)) == SHAPE      # row narrower than heads
+    assert call(img=stream(20 * A, ld=3 * 24 * 128 + 8)) == SHAPE   # stride not 16 values
+    assert call(txt=stream(10 * A, tokens=-1)) == SHAPE
+    assert call(txt=stream(10 * A, tokens=0), img=stream(20 * A, tokens=0), jq=None) == OK
+    assert call(img=stream(20 * A, eps=0.0)) == VALUE
+    assert call(img=stream(20 * A, eps=float("nan"))) == VALUE
+    assert call(jk=None) == NULL
+    assert call(jq=A + 16) == ALIGN
+    assert call(txt=stream(10 * A + 16)) == ALIGN
+    assert call(jk=A + 4096) == ALIAS                                # outputs overlap
+    assert call(jv=10 * A + 256) == ALIAS                            # output over text q
+    assert call(jq=20 * A + 100 * A + 64) == ALIAS                  # output over a weight

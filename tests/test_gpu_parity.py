@@ -1,8 +1,9 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle, element by element.
 
 Acceptance (per stage):
-  * bias_mul_add, token_cat_fp8, token_cat_nvfp4 (codes and block scales), residual_out:
-    bit-exact.
+  * bias_mul_add, token_cat_fp8, token_cat_nvfp4 (codes and block scales), residual_out,
+    the V copy of the QKV epilogue: bit-exact.
+  * QKV epilogue Q and K: at most one BF16 ulp against the oracle (counts reported).
   * quantise stage: q_gpu == E4M3(RN(y_gpu * inv)) bit-exact for every element (the
     oracle's quantise applied to the GPU's own y).
   * LayerNorm outputs: max |ulp| of y <= 1 against the oracle; q bit-exact wherever y
@@ -356,6 +357,84 @@ def test_token_cat_nvfp4_zero_rows_and_repeat_calls_agree():
     assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
     qr, sr = oracle.token_cat_nvfp4(a, inp["m"], 60.0)
     assert np.array_equal(q1, qr) and np.array_equal(s1, sr)
+
+
+# ------------------------------------------------------------------------------------------
+# QKV epilogue
+# ------------------------------------------------------------------------------------------
+
+def _dev_stream(st, heads, packed_dev=None):
+    """Device tensors for one stream: q, k, v as column slices of one packed tensor."""
+    packed = G.dev_bf16(st["packed"]) if packed_dev is None else packed_dev
+    hd = heads * 128
+    return dict(q=packed[:, :hd], k=packed[:, hd:2 * hd], v=packed[:, 2 * hd:3 * hd],
+                q_weight=G.dev_bf16(st["wq"]), k_weight=G.dev_bf16(st["wk"]),
+                cos_sin=torch.from_numpy(st["cos_sin"]).cuda(), eps=st["eps"])
+
+
+def run_qkv(d, heads):
+    tt, it = d["txt"]["q"].shape[0], d["img"]["q"].shape[0]
+    outs = [G.Guarded((tt + it, heads, 128), torch.bfloat16) for _ in range(3)]
+    fq().qkv_epilogue(_dev_stream(d["txt"], heads), _dev_stream(d["img"], heads), heads,
+                      out=tuple(o.tensor for o in outs))
+    torch.cuda.synchronize()
+    assert all(o.intact() for o in outs)
+    return [G.host_u16(o.tensor) for o in outs]
+
+
+def check_qkv(d, heads, what=""):
+    gq, gk, gv = run_qkv(d, heads)
+    rq, rk, rv = oracle.qkv_epilogue(d["txt"], d["img"], heads)
+    assert np.array_equal(gv, rv), f"{what}: v copy differs"
+    from tests.conftest import PARITY_COUNTS
+    for name, g_, r_ in (("q", gq, rq), ("k", gk, rk)):
+        diff = G.bf16_ulp_diff(g_, r_)
+        nmis = int((diff != 0).sum())
+        assert diff.max(initial=0) <= MAX_Y_ULP, f"{what} {name}: max ulp {diff.max()} ({nmis})"
+        PARITY_COUNTS.append((f"qkv {what} {name}", nmis, int(g_.size)))
+
+
+@pytest.mark.parametrize("name", ["qkv_qwen", "qkv_flux"])
+def test_qkv_epilogue_configs(name):
+    c = W.CONFIGS[name]
+    check_qkv(W.config_inputs(name), c["heads"], name)
+
+
+@pytest.mark.parametrize("tt,it,heads,extra", [(0, 64, 24, 0), (37, 0, 24, 0), (3, 5, 1, 16),
+                                               (2, 9, 5, 48), (7, 4, 7, 0), (1, 1, 13, 16),
+                                               (16, 16, 96, 0)])
+def test_qkv_epilogue_shapes(tt, it, heads, extra):
+    d = W.qkv_inputs(tt, it, heads, seed=tt * 31 + it + heads, extra_cols=extra)
+    d["img"]["eps"] = 1e-5
+    check_qkv(d, heads, f"{tt}+{it}x{heads}")
+
+
+def test_qkv_epilogue_special_heads():
+    """Zero heads, constant heads, tiny and huge magnitudes, exact midpoint products,
+    right-angle and identity rotations."""
+    heads = 8
+    d = W.qkv_inputs(3, 6, heads, seed=77)
+    for st in (d["txt"], d["img"]):
+        p = st["packed"]
+        q = p[:, :heads * 128].reshape(p.shape[0], heads, 128)
+        q[0, 0] = 0                                    # all-zero head (eps only)
+        q[0, 1] = W.to_bf16_bits(torch.tensor([1.5]))[0]   # constant head
+        q[1, 2] = W.to_bf16_bits(torch.randn(128) * 1e-12)
+        q[1, 3] = W.to_bf16_bits(torch.randn(128) * 1e15)
+        q[2, 4] = 0x8000                               # all -0
+        st["q"], st["k"], st["v"] = (p[:, :heads * 128], p[:, heads * 128:2 * heads * 128],
+                                     p[:, 2 * heads * 128:3 * heads * 128])
+        cs = st["cos_sin"]
+        cs[0, :64], cs[0, 64:] = 1.0, 0.0              # identity
+        cs[1, :64], cs[1, 64:] = 0.0, 1.0              # 90 degrees
+    check_qkv(d, heads, "specials")
+
+
+def test_qkv_epilogue_repeat_calls_agree():
+    d = W.config_inputs("qkv_qwen")
+    a = run_qkv(d, 24)
+    b = run_qkv(d, 24)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
 
 
 # ------------------------------------------------------------------------------------------
