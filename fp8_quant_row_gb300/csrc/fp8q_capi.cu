@@ -5,6 +5,7 @@
 // allocates device memory or synchronises, so the calls can be captured in CUDA graphs
 // once the per-device launch caches below are warm (first call on a device queries
 // attributes).
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -483,6 +484,28 @@ fp8q_status fp8q_qkv_epilogue(void* joint_q, void* joint_k, void* joint_v,
     dstp[i]->eps = st[i]->eps;
   }
   p.heads = int(heads);
+  if (heads <= fp8q::kQkvRingMaxHeads) {
+    // token ring: as many slots (2..4) as keep two CTAs per SM, else one CTA with 2..4 slots
+    const size_t stage = size_t(3 * heads * 256 + 512);
+    int stages = 4;
+    while (stages > 2 && 1024 + stages * stage > size_t(dev->smem_optin) / 2 - 1024) --stages;
+    if (1024 + stages * stage > size_t(dev->smem_optin) / 2 - 1024) {
+      stages = 4;
+      while (stages > 2 && 1024 + stages * stage > size_t(dev->smem_optin)) --stages;
+    }
+    const size_t smem = 1024 + stages * stage;
+    if (smem <= size_t(dev->smem_optin)) {
+      auto* fn = fp8q::qkv_ring_kernel;
+      int bps = 0;
+      stt = blocks_per_sm(reinterpret_cast<const void*>(fn), fp8q::kQkvRingWarps * 32, smem, &bps);
+      if (stt != FP8Q_OK) return stt;
+      if (bps > 0) {
+        const int64_t grid = std::min<int64_t>(total, int64_t(dev->sms) * bps);
+        return launch(fn, dim3(unsigned(grid)), dim3(fp8q::kQkvRingWarps * 32), smem, stream, p,
+                      stages);
+      }
+    }
+  }
   const unsigned gx = unsigned(total < 0x7FFFFFFF ? total : 0x7FFFFFFF);
   return launch(fp8q::qkv_epilogue_kernel, dim3(gx), dim3(fp8q::kQkvWarps * 32), 0, stream, p);
 }

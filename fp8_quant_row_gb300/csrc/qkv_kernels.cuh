@@ -33,6 +33,7 @@ namespace fp8q {
 
 constexpr int kQkvWarps = 6;       // per CTA: 2 x (Q, K, V)
 constexpr int kQkvBatch = 3;       // heads-of-four loaded ahead per Q/K warp
+constexpr int kQkvMinCtas = 4;     // resident CTAs per SM the register budget must allow
 constexpr int kHeadDim = 128;
 
 struct QkvStream {
@@ -128,10 +129,10 @@ __device__ __noinline__ uint32_t scaled_exact_bits(float p, float r_hi, float r_
   return pack_bf16x2(t_hi, 0.0f) & 0xFFFFu;
 }
 
-// RMSNorm + RoPE of this lane's 16 values (8 pairs); x, wt: packed BF16 words; c, s: the
-// lane's 8 cos and 8 sin values. Returns the 8 output words.
+// RMSNorm + RoPE of this lane's 16 values (8 pairs); x, wt: packed BF16 words; cw, sw: the
+// lane's 8 cos and 8 sin values (fp32 bits). Returns the 8 output words.
 __device__ __forceinline__ void qk_lane(const uint32_t (&x)[8], const uint32_t (&wt)[8],
-                                        const float (&c)[8], const float (&s)[8], dd r,
+                                        const uint32_t (&cw)[8], const uint32_t (&sw)[8], dd r,
                                         uint32_t (&o)[8]) {
   const f2 rh = f2_make(r.hi, r.hi), rl = f2_make(r.lo, r.lo);
   uint32_t n[8];
@@ -150,13 +151,14 @@ __device__ __forceinline__ void qk_lane(const uint32_t (&x)[8], const uint32_t (
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float a = bf_lo(n[i]), b = bf_hi(n[i]);        // (n[2i], n[2i+1])
-    const float o0 = __fsub_rn(__fmul_rn(a, c[i]), __fmul_rn(b, s[i]));
-    const float o1 = __fadd_rn(__fmul_rn(b, c[i]), __fmul_rn(a, s[i]));
+    const float c = __uint_as_float(cw[i]), s = __uint_as_float(sw[i]);
+    const float o0 = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
+    const float o1 = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, s));
     o[i] = pack_bf16x2(o0, o1);
   }
 }
 
-__global__ void __launch_bounds__(kQkvWarps * 32) qkv_epilogue_kernel(QkvParams P) {
+__global__ void __launch_bounds__(kQkvWarps * 32, kQkvMinCtas) qkv_epilogue_kernel(QkvParams P) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kind = warp >> 1;       // 0: Q, 1: K, 2: V
   const int first_quad = warp & 1;  // the two warps of a kind take alternate heads-of-four
@@ -196,20 +198,8 @@ __global__ void __launch_bounds__(kQkvWarps * 32) qkv_epilogue_kernel(QkvParams 
       continue;
     }
     const float eps = sel(P.txt.eps, P.img.eps);
-    uint32_t wt[8];
-    ld_nc32((kind == 0 ? sel(P.txt.wq, P.img.wq) : sel(P.txt.wk, P.img.wk)) + u * 16, wt);
-    float c[8], s[8];
-    {
-      uint32_t cw[8], sw[8];
-      const float* cs = sel(P.txt.cos_sin, P.img.cos_sin) + row * kHeadDim + u * 8;
-      ld_nc32(cs, cw);
-      ld_nc32(cs + 64, sw);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        c[i] = __uint_as_float(cw[i]);
-        s[i] = __uint_as_float(sw[i]);
-      }
-    }
+    const uint16_t* wsrc = (kind == 0 ? sel(P.txt.wq, P.img.wq) : sel(P.txt.wk, P.img.wk)) + u * 16;
+    const float* cs = sel(P.txt.cos_sin, P.img.cos_sin) + row * kHeadDim + u * 8;
     for (int qd0 = first_quad; qd0 < quads; qd0 += 2 * kQkvBatch) {
       uint32_t x[kQkvBatch][8];
 #pragma unroll
@@ -226,13 +216,151 @@ __global__ void __launch_bounds__(kQkvWarps * 32) qkv_epilogue_kernel(QkvParams 
       for (int b = 0; b < kQkvBatch; ++b) {
         if (qd0 + 2 * b >= quads) break;  // warp-uniform
         const dd r = head_rrms(x[b], eps);
+        // weight and cos/sin are re-read per head (L1 hits) rather than held in registers
+        uint32_t wt[8], cw[8], sw[8];
+        ld_nc32(wsrc, wt);
+        ld_nc32(cs, cw);
+        ld_nc32(cs + 64, sw);
         uint32_t o[8];
-        qk_lane(x[b], wt, c, s, r, o);
+        qk_lane(x[b], wt, cw, sw, r, o);
         const int h = (qd0 + 2 * b) * 4 + g;
         if (h < heads) st_stream32(dst + h * kHeadDim, o);
       }
     }
   }
+}
+
+// ------------------------------------------------------------------------------------------
+// Ring kernel (heads <= 64): persistent CTAs stream whole tokens through a cp.async ring
+// ------------------------------------------------------------------------------------------
+//
+// Shared memory: the four RMSNorm weights (text q, k, image q, k; 256 B each), then `stages`
+// token slots of q | k | v (heads x 256 B each) | cos/sin row (512 B). Every thread copies its
+// share of a token with 16-byte cp.async; a slot is issued `stages - 1` tokens ahead, so the
+// bytes in flight do not depend on registers. Per token: V goes shared -> global as 16-byte
+// chunks; each warp normalises and rotates one heads-of-four of Q or K at a time from shared
+// memory and stores its 32 bytes per lane straight to global memory.
+constexpr int kQkvRingWarps = 12;
+constexpr int kQkvRingMaxHeads = 64;
+
+__device__ __forceinline__ void st_global16(void* p, float4 v) {
+  __stcs(reinterpret_cast<float4*>(p), v);
+}
+
+// A lane's 32 bytes from shared memory as 8 words; lanes whose 32-byte index has bit 2 set
+// read the upper half first, so the 8 lanes of a shared-memory phase hit 32 distinct banks.
+__device__ __forceinline__ void lds32B(const uint8_t* p, int lane, uint32_t (&w)[8]) {
+  const bool swap = (lane >> 2) & 1;
+  const float4 a = lds128(reinterpret_cast<const float4*>(p + (swap ? 16 : 0)));
+  const float4 b = lds128(reinterpret_cast<const float4*>(p + (swap ? 0 : 16)));
+  const float4 lo = swap ? b : a, hi = swap ? a : b;
+  w[0] = __float_as_uint(lo.x); w[1] = __float_as_uint(lo.y);
+  w[2] = __float_as_uint(lo.z); w[3] = __float_as_uint(lo.w);
+  w[4] = __float_as_uint(hi.x); w[5] = __float_as_uint(hi.y);
+  w[6] = __float_as_uint(hi.z); w[7] = __float_as_uint(hi.w);
+}
+
+__device__ __forceinline__ void cp_async_wait_dyn(int pending) {
+  switch (pending) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    default: cp_async_wait<3>(); break;
+  }
+}
+
+__global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams P, int stages) {
+  extern __shared__ __align__(16) uint8_t qkv_smem[];
+  const int H = P.heads;
+  const int row_bytes = H * 256;
+  const int stage_bytes = 3 * row_bytes + 512;
+  uint8_t* wsm = qkv_smem;
+  uint8_t* ring = qkv_smem + 1024;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 3, u = lane & 7;
+  const int quads = (H + 3) >> 2;
+  const int64_t row_len = int64_t(H) * kHeadDim;
+  const int64_t total = P.txt.tokens + P.img.tokens;
+  const int chunks_qkv = 3 * H * 16;
+  wait_for_producers();
+
+  if (tid < 64) {  // the four weight vectors (a stream without tokens has none)
+    const int w = tid >> 4, c = tid & 15;
+    const uint16_t* src = w == 0 ? P.txt.wq : w == 1 ? P.txt.wk : w == 2 ? P.img.wq : P.img.wk;
+    const bool present = (w < 2 ? P.txt.tokens : P.img.tokens) > 0;
+    if (present) cp_async16(wsm + w * 256 + c * 16, src + c * 8);
+  }
+
+  auto issue = [&](int64_t jt, int slot) {
+    const bool is_txt = jt < P.txt.tokens;
+    auto sel = [is_txt](auto a, auto b) { return is_txt ? a : b; };
+    const int64_t row = is_txt ? jt : jt - P.txt.tokens;
+    const int64_t roff = row * sel(P.txt.ld, P.img.ld);
+    const uint16_t* qs = sel(P.txt.q, P.img.q) + roff;
+    const uint16_t* ks = sel(P.txt.k, P.img.k) + roff;
+    const uint16_t* vs = sel(P.txt.v, P.img.v) + roff;
+    const float* cs = sel(P.txt.cos_sin, P.img.cos_sin) + row * kHeadDim;
+    uint8_t* dst = ring + slot * stage_bytes;
+    for (int c = tid; c < chunks_qkv + 32; c += kQkvRingWarps * 32) {
+      if (c < chunks_qkv) {
+        const int kind = c / (H * 16), off = c - kind * (H * 16);
+        const uint16_t* src = (kind == 0 ? qs : kind == 1 ? ks : vs) + off * 8;
+        cp_async16(dst + kind * row_bytes + off * 16, src);
+      } else {
+        const int off = c - chunks_qkv;
+        cp_async16(dst + 3 * row_bytes + off * 16, cs + off * 4);
+      }
+    }
+  };
+
+  const int64_t stride = gridDim.x;
+  for (int sidx = 0; sidx < stages - 1; ++sidx) {
+    const int64_t jt = blockIdx.x + sidx * stride;
+    if (jt < total) issue(jt, sidx);
+    cp_async_commit();  // the weights ride in the first group
+  }
+  for (int64_t it = 0;; ++it) {
+    const int64_t jt = blockIdx.x + it * stride;
+    if (jt >= total) break;
+    {
+      const int64_t jn = blockIdx.x + (it + stages - 1) * stride;
+      if (jn < total) issue(jn, int((it + stages - 1) % stages));
+      cp_async_commit();
+    }
+    cp_async_wait_dyn(stages - 1);
+    __syncthreads();
+    const uint8_t* st = ring + int(it % stages) * stage_bytes;
+    const bool is_txt = jt < P.txt.tokens;
+
+    // V: shared -> global
+    for (int c = tid; c < H * 16; c += kQkvRingWarps * 32)
+      st_global16(P.jv + jt * row_len + c * 8,
+                  lds128(reinterpret_cast<const float4*>(st + 2 * row_bytes + c * 16)));
+
+    // Q, K: one heads-of-four per warp at a time
+    const float eps = is_txt ? P.txt.eps : P.img.eps;
+    for (int qq = warp; qq < 2 * quads; qq += kQkvRingWarps) {
+      const int kind = qq >= quads;          // 0: Q, 1: K
+      const int h = (qq - kind * quads) * 4 + g;
+      uint32_t x[8];
+      if (h < H) {
+        lds32B(st + kind * row_bytes + h * 256 + u * 32, lane, x);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = 0u;
+      }
+      const dd r = head_rrms(x, eps);
+      uint32_t wt[8], cw[8], sw[8];
+      lds32B(wsm + ((is_txt ? 0 : 2) + kind) * 256 + u * 32, lane, wt);
+      lds32B(st + 3 * row_bytes + u * 32, lane, cw);
+      lds32B(st + 3 * row_bytes + 256 + u * 32, lane, sw);
+      uint32_t o[8];
+      qk_lane(x, wt, cw, sw, r, o);
+      if (h < H) st_stream32((kind == 0 ? P.jq : P.jk) + jt * row_len + h * kHeadDim + u * 16, o);
+    }
+    __syncthreads();  // the slot may be refilled from the next iteration on
+  }
+  cp_async_wait<0>();
 }
 
 }  // namespace fp8q
