@@ -485,25 +485,17 @@ fp8q_status fp8q_qkv_epilogue(void* joint_q, void* joint_k, void* joint_v,
   }
   p.heads = int(heads);
   if (heads <= fp8q::kQkvRingMaxHeads) {
-    // token ring: as many slots (2..4) as keep two CTAs per SM, else one CTA with 2..4 slots
-    const size_t stage = size_t(3 * heads * 256 + 512);
-    int stages = 4;
-    while (stages > 2 && 1024 + stages * stage > size_t(dev->smem_optin) / 2 - 1024) --stages;
-    if (1024 + stages * stage > size_t(dev->smem_optin) / 2 - 1024) {
-      stages = 4;
-      while (stages > 2 && 1024 + stages * stage > size_t(dev->smem_optin)) --stages;
-    }
-    const size_t smem = 1024 + stages * stage;
-    if (smem <= size_t(dev->smem_optin)) {
-      auto* fn = fp8q::qkv_ring_kernel;
-      int bps = 0;
-      stt = blocks_per_sm(reinterpret_cast<const void*>(fn), fp8q::kQkvRingWarps * 32, smem, &bps);
-      if (stt != FP8Q_OK) return stt;
-      if (bps > 0) {
-        const int64_t grid = std::min<int64_t>(total, int64_t(dev->sms) * bps);
-        return launch(fn, dim3(unsigned(grid)), dim3(fp8q::kQkvRingWarps * 32), smem, stream, p,
-                      stages);
-      }
+    // per-warp item pipelines; two or more CTAs per SM
+    const size_t smem = 1024 + size_t(fp8q::kQkvRingWarps) * fp8q::kQkvDepth * fp8q::kQkvSlotBytes;
+    auto* fn = fp8q::qkv_ring_kernel;
+    int bps = 0;
+    stt = blocks_per_sm(reinterpret_cast<const void*>(fn), fp8q::kQkvRingWarps * 32, smem, &bps);
+    if (stt != FP8Q_OK) return stt;
+    if (bps > 0) {
+      const int64_t items = total * 3 * ((heads + 7) / 8);
+      const int64_t need = (items + fp8q::kQkvRingWarps - 1) / fp8q::kQkvRingWarps;
+      const int64_t grid = std::min<int64_t>(need, int64_t(dev->sms) * bps);
+      return launch(fn, dim3(unsigned(grid)), dim3(fp8q::kQkvRingWarps * 32), smem, stream, p);
     }
   }
   const unsigned gx = unsigned(total < 0x7FFFFFFF ? total : 0x7FFFFFFF);

@@ -234,30 +234,25 @@ __global__ void __launch_bounds__(kQkvWarps * 32, kQkvMinCtas) qkv_epilogue_kern
 // Ring kernel (heads <= 64): persistent CTAs stream whole tokens through a cp.async ring
 // ------------------------------------------------------------------------------------------
 //
-// Shared memory: the four RMSNorm weights (text q, k, image q, k; 256 B each), then `stages`
-// token slots of q | k | v (heads x 256 B each) | cos/sin row (512 B). Every thread copies its
-// share of a token with 16-byte cp.async; a slot is issued `stages - 1` tokens ahead, so the
-// bytes in flight do not depend on registers. Per token: V goes shared -> global as 16-byte
-// chunks; each warp normalises and rotates one heads-of-four of Q or K at a time from shared
-// memory and stores its 32 bytes per lane straight to global memory.
-constexpr int kQkvRingWarps = 12;
+// Four lanes per head, 32 values (16 packed words, 16 RoPE pairs) per lane, eight heads per
+// warp: the per-head work (reductions, double-float constants) is shared by 32 values.
+// Shared memory: the four RMSNorm weights (text q, k, image q, k; planar), then per warp
+// `kQkvDepth` slots. q, k, the weights and cos/sin are stored in four planes: 16-byte chunk j
+// of every 64-byte lane segment goes to plane j, so a warp's 16-byte loads of one plane are
+// contiguous (no bank conflicts); v is stored as is.
+constexpr int kQkvRingWarps = 8;
 constexpr int kQkvRingMaxHeads = 64;
 
 __device__ __forceinline__ void st_global16(void* p, float4 v) {
   __stcs(reinterpret_cast<float4*>(p), v);
 }
 
-// A lane's 32 bytes from shared memory as 8 words; lanes whose 32-byte index has bit 2 set
-// read the upper half first, so the 8 lanes of a shared-memory phase hit 32 distinct banks.
-__device__ __forceinline__ void lds32B(const uint8_t* p, int lane, uint32_t (&w)[8]) {
-  const bool swap = (lane >> 2) & 1;
-  const float4 a = lds128(reinterpret_cast<const float4*>(p + (swap ? 16 : 0)));
-  const float4 b = lds128(reinterpret_cast<const float4*>(p + (swap ? 0 : 16)));
-  const float4 lo = swap ? b : a, hi = swap ? a : b;
-  w[0] = __float_as_uint(lo.x); w[1] = __float_as_uint(lo.y);
-  w[2] = __float_as_uint(lo.z); w[3] = __float_as_uint(lo.w);
-  w[4] = __float_as_uint(hi.x); w[5] = __float_as_uint(hi.y);
-  w[6] = __float_as_uint(hi.z); w[7] = __float_as_uint(hi.w);
+__device__ __forceinline__ void lds_words4(const uint8_t* p, uint32_t* w) {
+  const float4 v = lds128(reinterpret_cast<const float4*>(p));
+  w[0] = __float_as_uint(v.x);
+  w[1] = __float_as_uint(v.y);
+  w[2] = __float_as_uint(v.z);
+  w[3] = __float_as_uint(v.w);
 }
 
 __device__ __forceinline__ void cp_async_wait_dyn(int pending) {
@@ -269,96 +264,230 @@ __device__ __forceinline__ void cp_async_wait_dyn(int pending) {
   }
 }
 
-__global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams P, int stages) {
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// 1 / sqrt(sum(x^2) / 128 + eps) for the head held by this lane's group of 4 lanes (32 values
+// each), with the same exact accumulation as head_rrms.
+__device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], float eps) {
+  uint32_t m = absmax_bf16x2(w[0], w[1]);
+#pragma unroll
+  for (int i = 2; i < 16; ++i) m = absmax_bf16x2(m, w[i]);
+  uint32_t mx = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
+  mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+  mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+  const int E = min(max(int(mx >> 7) - 127, -40), 56);
+  const float K2 = exp2i(2 * E + 9);
+  const float K3 = 1.5f * exp2i(2 * E - 9);  // 48 u, u = 2^(2E - 14)
+  f2 S = f2_make(K2, K2), R = f2_make(K3, K3), T = f2_make(0.0f, 0.0f);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const f2 v = bf2_to_f2(w[i]);
+    const f2 sn = fma2(v, v, S);
+    const f2 e = fma2(v, v, sub2(S, sn));  // exact error of sn
+    S = sn;
+    const f2 r = add2(R, e);
+    T = add2(T, sub2(e, sub2(r, R)));     // FastTwoSum error (|R| > |e|)
+    R = r;
+  }
+  const float inv_u = exp2i(14 - 2 * E);
+  int cs = __float2int_rn(__fmul_rn(__fsub_rn(f2_lo(S), K2), inv_u)) +
+           __float2int_rn(__fmul_rn(__fsub_rn(f2_hi(S), K2), inv_u));
+  const float inv_u2 = exp2i(32 - 2 * E);
+  int cr = __float2int_rn(__fmul_rn(__fsub_rn(f2_lo(R), K3), inv_u2)) +
+           __float2int_rn(__fmul_rn(__fsub_rn(f2_hi(R), K3), inv_u2));
+  float t = __fadd_rn(f2_lo(T), f2_hi(T));
+#pragma unroll
+  for (int o = 1; o < 4; o <<= 1) {
+    cs += __shfl_xor_sync(0xFFFFFFFFu, cs, o);
+    cr += __shfl_xor_sync(0xFFFFFFFFu, cr, o);
+    t = __fadd_rn(t, __shfl_xor_sync(0xFFFFFFFFu, t, o));
+  }
+  dd sum = dd_add(int_to_dd(cs, exp2i(2 * E - 14)), int_to_dd(cr, exp2i(2 * E - 32)));
+  sum = dd_add(sum, dd{t, 0.0f});
+  const dd ms = dd{__fmul_rn(sum.hi, 1.0f / kHeadDim), __fmul_rn(sum.lo, 1.0f / kHeadDim)};
+  return dd_rsqrt(dd_add(ms, dd{eps, 0.0f}));
+}
+
+// Normalised words n = RN_bf16(x w r) for one packed word; sets `unsure` when the fast value
+// could round the other way (the bracket t (1 +- 2^-20), wider than the fast path's error,
+// rounds to two different BF16 pairs).
+__device__ __forceinline__ uint32_t norm_word(uint32_t xw, uint32_t ww, f2 rh, f2 rl,
+                                              bool& unsure) {
+  const f2 p = mul2(bf2_to_f2(xw), bf2_to_f2(ww));  // exact
+  const f2 t = fma2(p, rh, mul2(p, rl));
+  const f2 up = fma2(t, f2_make(0x1p-20f, 0x1p-20f), t);
+  const f2 dn = fma2(t, f2_make(-0x1p-20f, -0x1p-20f), t);
+  unsure |= pack_bf16x2(f2_lo(up), f2_hi(up)) != pack_bf16x2(f2_lo(dn), f2_hi(dn));
+  return pack_bf16x2(f2_lo(t), f2_hi(t));
+}
+
+__device__ __noinline__ uint32_t norm_word_exact(uint32_t xw, uint32_t ww, float r_hi,
+                                                 float r_lo) {
+  const float p0 = __fmul_rn(bf_lo(xw), bf_lo(ww)), p1 = __fmul_rn(bf_hi(xw), bf_hi(ww));
+  return scaled_exact_bits(p0, r_hi, r_lo) | (scaled_exact_bits(p1, r_hi, r_lo) << 16);
+}
+
+__device__ __forceinline__ uint32_t rope_word(uint32_t nw, float c, float s) {
+  const float a = bf_lo(nw), b = bf_hi(nw);
+  return pack_bf16x2(__fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)),
+                     __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, s)));
+}
+
+// Each warp runs its own pipeline over a flat list of work items, `kQkvDepth - 1` items
+// ahead, with no CTA-wide barrier after the start: item = (token, type), type one of the
+// eight-head blocks of Q, of K or of V. A Q/K item brings 2 KB of values (planar) and the
+// token's cos/sin row into the warp's slot; a V item brings 2 KB that go straight back out.
+constexpr int kQkvDepth = 4;           // slots per warp
+constexpr int kQkvSlotBytes = 2560;    // 8 heads x 256 B + cos/sin 512 B
+
+__global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams P) {
   extern __shared__ __align__(16) uint8_t qkv_smem[];
   const int H = P.heads;
-  const int row_bytes = H * 256;
-  const int stage_bytes = 3 * row_bytes + 512;
-  uint8_t* wsm = qkv_smem;
-  uint8_t* ring = qkv_smem + 1024;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 3, u = lane & 7;
-  const int quads = (H + 3) >> 2;
+  const int g8 = lane >> 2, qtr = lane & 3;
+  const int octs = (H + 7) >> 3;
+  const int per_token = 3 * octs;
   const int64_t row_len = int64_t(H) * kHeadDim;
-  const int64_t total = P.txt.tokens + P.img.tokens;
-  const int chunks_qkv = 3 * H * 16;
+  const int64_t total_items = (P.txt.tokens + P.img.tokens) * per_token;
+  uint8_t* wsm = qkv_smem;
+  uint8_t* ring = qkv_smem + 1024 + warp * (kQkvDepth * kQkvSlotBytes);
   wait_for_producers();
 
-  if (tid < 64) {  // the four weight vectors (a stream without tokens has none)
+  if (tid < 64) {  // the four weight vectors, planar (a stream without tokens has none)
     const int w = tid >> 4, c = tid & 15;
     const uint16_t* src = w == 0 ? P.txt.wq : w == 1 ? P.txt.wk : w == 2 ? P.img.wq : P.img.wk;
     const bool present = (w < 2 ? P.txt.tokens : P.img.tokens) > 0;
-    if (present) cp_async16(wsm + w * 256 + c * 16, src + c * 8);
+    if (present) cp_async16(wsm + w * 256 + (c & 3) * 64 + (c >> 2) * 16, src + c * 8);
   }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
 
-  auto issue = [&](int64_t jt, int slot) {
-    const bool is_txt = jt < P.txt.tokens;
+  struct Item {
+    int64_t token;
+    int type;  // 0: Q, 1: K, 2: V
+    int oc;    // eight-head block
+  };
+  auto decode = [&](int64_t item) {
+    Item it;
+    it.token = item / per_token;
+    const int r = int(item - it.token * per_token);
+    it.type = r / octs;
+    it.oc = r - it.type * octs;
+    return it;
+  };
+  auto issue = [&](int64_t item, int slot) {
+    const Item it = decode(item);
+    const bool is_txt = it.token < P.txt.tokens;
     auto sel = [is_txt](auto a, auto b) { return is_txt ? a : b; };
-    const int64_t row = is_txt ? jt : jt - P.txt.tokens;
-    const int64_t roff = row * sel(P.txt.ld, P.img.ld);
-    const uint16_t* qs = sel(P.txt.q, P.img.q) + roff;
-    const uint16_t* ks = sel(P.txt.k, P.img.k) + roff;
-    const uint16_t* vs = sel(P.txt.v, P.img.v) + roff;
-    const float* cs = sel(P.txt.cos_sin, P.img.cos_sin) + row * kHeadDim;
-    uint8_t* dst = ring + slot * stage_bytes;
-    for (int c = tid; c < chunks_qkv + 32; c += kQkvRingWarps * 32) {
-      if (c < chunks_qkv) {
-        const int kind = c / (H * 16), off = c - kind * (H * 16);
-        const uint16_t* src = (kind == 0 ? qs : kind == 1 ? ks : vs) + off * 8;
-        cp_async16(dst + kind * row_bytes + off * 16, src);
-      } else {
-        const int off = c - chunks_qkv;
-        cp_async16(dst + 3 * row_bytes + off * 16, cs + off * 4);
+    const int64_t row = is_txt ? it.token : it.token - P.txt.tokens;
+    const uint16_t* base = it.type == 0 ? sel(P.txt.q, P.img.q)
+                         : it.type == 1 ? sel(P.txt.k, P.img.k) : sel(P.txt.v, P.img.v);
+    const uint16_t* src = base + row * sel(P.txt.ld, P.img.ld) + it.oc * 8 * kHeadDim;
+    uint8_t* dst = ring + slot * kQkvSlotBytes;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int c = lane + 32 * k;          // 16-byte chunk of the 2 KB block
+      const int hh = c >> 4, c16 = c & 15;  // head in the block, chunk in the head
+      if (it.oc * 8 + hh < H) {
+        const int off = it.type == 2 ? c * 16 : (c16 & 3) * 512 + (hh * 4 + (c16 >> 2)) * 16;
+        cp_async16(dst + off, src + c * 8);
       }
+    }
+    if (it.type != 2) {  // cos (lanes 0..15) and sin (16..31), planar within each 256 bytes
+      const float* cs = sel(P.txt.cos_sin, P.img.cos_sin) + row * kHeadDim;
+      const int half = lane >> 4, k = lane & 15;
+      cp_async16(dst + 2048 + half * 256 + (k & 3) * 64 + (k >> 2) * 16, cs + lane * 4);
     }
   };
 
-  const int64_t stride = gridDim.x;
-  for (int sidx = 0; sidx < stages - 1; ++sidx) {
-    const int64_t jt = blockIdx.x + sidx * stride;
-    if (jt < total) issue(jt, sidx);
-    cp_async_commit();  // the weights ride in the first group
+  const int64_t gw = int64_t(blockIdx.x) * kQkvRingWarps + warp;
+  const int64_t W = int64_t(gridDim.x) * kQkvRingWarps;
+#pragma unroll
+  for (int k = 0; k < kQkvDepth - 1; ++k) {
+    const int64_t item = gw + k * W;
+    if (item < total_items) issue(item, k);
+    cp_async_commit();
   }
-  for (int64_t it = 0;; ++it) {
-    const int64_t jt = blockIdx.x + it * stride;
-    if (jt >= total) break;
+  for (int64_t k = 0;; ++k) {
+    const int64_t item = gw + k * W;
+    if (item >= total_items) break;
     {
-      const int64_t jn = blockIdx.x + (it + stages - 1) * stride;
-      if (jn < total) issue(jn, int((it + stages - 1) % stages));
+      const int64_t next = gw + (k + kQkvDepth - 1) * W;
+      if (next < total_items) issue(next, int((k + kQkvDepth - 1) % kQkvDepth));
       cp_async_commit();
     }
-    cp_async_wait_dyn(stages - 1);
-    __syncthreads();
-    const uint8_t* st = ring + int(it % stages) * stage_bytes;
-    const bool is_txt = jt < P.txt.tokens;
-
-    // V: shared -> global
-    for (int c = tid; c < H * 16; c += kQkvRingWarps * 32)
-      st_global16(P.jv + jt * row_len + c * 8,
-                  lds128(reinterpret_cast<const float4*>(st + 2 * row_bytes + c * 16)));
-
-    // Q, K: one heads-of-four per warp at a time
-    const float eps = is_txt ? P.txt.eps : P.img.eps;
-    for (int qq = warp; qq < 2 * quads; qq += kQkvRingWarps) {
-      const int kind = qq >= quads;          // 0: Q, 1: K
-      const int h = (qq - kind * quads) * 4 + g;
-      uint32_t x[8];
-      if (h < H) {
-        lds32B(st + kind * row_bytes + h * 256 + u * 32, lane, x);
-      } else {
+    cp_async_wait<kQkvDepth - 1>();
+    __syncwarp();
+    const uint8_t* sl = ring + int(k % kQkvDepth) * kQkvSlotBytes;
+    const Item it = decode(item);
+    const bool is_txt = it.token < P.txt.tokens;
+    if (it.type == 2) {
+      uint16_t* dst = P.jv + it.token * row_len + it.oc * 8 * kHeadDim;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = 0u;
+      for (int kk = 0; kk < 4; ++kk) {
+        const int c = lane + 32 * kk;
+        if (it.oc * 8 + (c >> 4) < H)
+          st_global16(dst + c * 8, lds128(reinterpret_cast<const float4*>(sl + c * 16)));
       }
-      const dd r = head_rrms(x, eps);
-      uint32_t wt[8], cw[8], sw[8];
-      lds32B(wsm + ((is_txt ? 0 : 2) + kind) * 256 + u * 32, lane, wt);
-      lds32B(st + 3 * row_bytes + u * 32, lane, cw);
-      lds32B(st + 3 * row_bytes + 256 + u * 32, lane, sw);
-      uint32_t o[8];
-      qk_lane(x, wt, cw, sw, r, o);
-      if (h < H) st_stream32((kind == 0 ? P.jq : P.jk) + jt * row_len + h * kHeadDim + u * 16, o);
+    } else {
+      const int h = it.oc * 8 + g8;
+      uint32_t x[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (h < H) {
+          lds_words4(sl + j * 512 + (g8 * 4 + qtr) * 16, x + 4 * j);
+        } else {
+          x[4 * j] = x[4 * j + 1] = x[4 * j + 2] = x[4 * j + 3] = 0u;
+        }
+      }
+      const dd r = head_rrms4(x, is_txt ? P.txt.eps : P.img.eps);
+      const f2 rh = f2_make(r.hi, r.hi), rl = f2_make(r.lo, r.lo);
+      const uint8_t* wv = wsm + ((is_txt ? 0 : 2) + it.type) * 256 + qtr * 16;
+      uint32_t n[16];
+      bool unsure = false;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t wt[4];
+        lds_words4(wv + j * 64, wt);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) n[4 * j + i] = norm_word(x[4 * j + i], wt[i], rh, rl, unsure);
+      }
+      if (unsure) {  // rare: redo the words whose bracket straddles a rounding boundary
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t wt[4];
+          lds_words4(wv + j * 64, wt);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            bool u1 = false;
+            norm_word(x[4 * j + i], wt[i], rh, rl, u1);
+            if (u1) n[4 * j + i] = norm_word_exact(x[4 * j + i], wt[i], r.hi, r.lo);
+          }
+        }
+      }
+      const uint8_t* csv = sl + 2048 + qtr * 16;
+      uint32_t o[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 c4 = lds128(reinterpret_cast<const float4*>(csv + j * 64));
+        const float4 s4 = lds128(reinterpret_cast<const float4*>(csv + 256 + j * 64));
+        o[4 * j + 0] = rope_word(n[4 * j + 0], c4.x, s4.x);
+        o[4 * j + 1] = rope_word(n[4 * j + 1], c4.y, s4.y);
+        o[4 * j + 2] = rope_word(n[4 * j + 2], c4.z, s4.z);
+        o[4 * j + 3] = rope_word(n[4 * j + 3], c4.w, s4.w);
+      }
+      if (h < H) {
+        uint16_t* dst = (it.type == 0 ? P.jq : P.jk) + it.token * row_len + h * kHeadDim + qtr * 32;
+        st_stream32(dst, *reinterpret_cast<const uint32_t(*)[8]>(o));
+        st_stream32(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(o + 8));
+      }
     }
-    __syncthreads();  // the slot may be refilled from the next iteration on
+    __syncwarp();  // every lane is done with the slot before it is refilled
   }
   cp_async_wait<0>();
 }
