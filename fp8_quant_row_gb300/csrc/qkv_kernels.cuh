@@ -352,7 +352,6 @@ __global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams 
   const int octs = (H + 7) >> 3;
   const int per_token = 3 * octs;
   const int64_t row_len = int64_t(H) * kHeadDim;
-  const int64_t total_items = (P.txt.tokens + P.img.tokens) * per_token;
   uint8_t* wsm = qkv_smem;
   uint8_t* ring = qkv_smem + 1024 + warp * (kQkvDepth * kQkvSlotBytes);
   wait_for_producers();
@@ -367,75 +366,78 @@ __global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams 
   cp_async_wait<0>();
   __syncthreads();
 
+  // Items gw, gw + W, gw + 2W, ... as (token, remainder) pairs, advanced without division.
   struct Item {
     int64_t token;
-    int type;  // 0: Q, 1: K, 2: V
-    int oc;    // eight-head block
+    int r;     // 0 .. per_token - 1: type = r / octs, eight-head block = r % octs
   };
-  auto decode = [&](int64_t item) {
-    Item it;
-    it.token = item / per_token;
-    const int r = int(item - it.token * per_token);
-    it.type = r / octs;
-    it.oc = r - it.type * octs;
-    return it;
+  const int64_t gw = int64_t(blockIdx.x) * kQkvRingWarps + warp;
+  const int64_t W = int64_t(gridDim.x) * kQkvRingWarps;
+  const int64_t w_tok = W / per_token;
+  const int w_rem = int(W - w_tok * per_token);
+  auto advance = [&](Item& it) {
+    it.token += w_tok;
+    it.r += w_rem;
+    if (it.r >= per_token) {
+      it.r -= per_token;
+      ++it.token;
+    }
   };
-  auto issue = [&](int64_t item, int slot) {
-    const Item it = decode(item);
+  const int64_t total_tokens = P.txt.tokens + P.img.tokens;
+  auto issue = [&](const Item& it, int slot) {
     const bool is_txt = it.token < P.txt.tokens;
     auto sel = [is_txt](auto a, auto b) { return is_txt ? a : b; };
     const int64_t row = is_txt ? it.token : it.token - P.txt.tokens;
-    const uint16_t* base = it.type == 0 ? sel(P.txt.q, P.img.q)
-                         : it.type == 1 ? sel(P.txt.k, P.img.k) : sel(P.txt.v, P.img.v);
-    const uint16_t* src = base + row * sel(P.txt.ld, P.img.ld) + it.oc * 8 * kHeadDim;
+    const int type = it.r / octs, oc = it.r - (it.r / octs) * octs;
+    const uint16_t* base = type == 0 ? sel(P.txt.q, P.img.q)
+                         : type == 1 ? sel(P.txt.k, P.img.k) : sel(P.txt.v, P.img.v);
+    const uint16_t* src = base + row * sel(P.txt.ld, P.img.ld) + oc * 8 * kHeadDim;
     uint8_t* dst = ring + slot * kQkvSlotBytes;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int c = lane + 32 * k;          // 16-byte chunk of the 2 KB block
       const int hh = c >> 4, c16 = c & 15;  // head in the block, chunk in the head
-      if (it.oc * 8 + hh < H) {
-        const int off = it.type == 2 ? c * 16 : (c16 & 3) * 512 + (hh * 4 + (c16 >> 2)) * 16;
+      if (oc * 8 + hh < H) {
+        const int off = type == 2 ? c * 16 : (c16 & 3) * 512 + (hh * 4 + (c16 >> 2)) * 16;
         cp_async16(dst + off, src + c * 8);
       }
     }
-    if (it.type != 2) {  // cos (lanes 0..15) and sin (16..31), planar within each 256 bytes
+    if (type != 2) {  // cos (lanes 0..15) and sin (16..31), planar within each 256 bytes
       const float* cs = sel(P.txt.cos_sin, P.img.cos_sin) + row * kHeadDim;
       const int half = lane >> 4, k = lane & 15;
       cp_async16(dst + 2048 + half * 256 + (k & 3) * 64 + (k >> 2) * 16, cs + lane * 4);
     }
   };
 
-  const int64_t gw = int64_t(blockIdx.x) * kQkvRingWarps + warp;
-  const int64_t W = int64_t(gridDim.x) * kQkvRingWarps;
+  // the item being processed and the one being issued (kQkvDepth - 1 items ahead)
+  Item cur{gw / per_token, int(gw % per_token)};
+  Item ahead = cur;
 #pragma unroll
   for (int k = 0; k < kQkvDepth - 1; ++k) {
-    const int64_t item = gw + k * W;
-    if (item < total_items) issue(item, k);
+    if (ahead.token < total_tokens) issue(ahead, k);
     cp_async_commit();
+    advance(ahead);
   }
-  for (int64_t k = 0;; ++k) {
-    const int64_t item = gw + k * W;
-    if (item >= total_items) break;
-    {
-      const int64_t next = gw + (k + kQkvDepth - 1) * W;
-      if (next < total_items) issue(next, int((k + kQkvDepth - 1) % kQkvDepth));
-      cp_async_commit();
-    }
+  for (int64_t k = 0; cur.token < total_tokens; ++k, advance(cur)) {
+    if (ahead.token < total_tokens) issue(ahead, int((k + kQkvDepth - 1) % kQkvDepth));
+    cp_async_commit();
+    advance(ahead);
     cp_async_wait<kQkvDepth - 1>();
     __syncwarp();
     const uint8_t* sl = ring + int(k % kQkvDepth) * kQkvSlotBytes;
-    const Item it = decode(item);
+    const Item it = cur;
+    const int type = it.r / octs, oc = it.r - type * octs;
     const bool is_txt = it.token < P.txt.tokens;
-    if (it.type == 2) {
-      uint16_t* dst = P.jv + it.token * row_len + it.oc * 8 * kHeadDim;
+    if (type == 2) {
+      uint16_t* dst = P.jv + it.token * row_len + oc * 8 * kHeadDim;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const int c = lane + 32 * kk;
-        if (it.oc * 8 + (c >> 4) < H)
+        if (oc * 8 + (c >> 4) < H)
           st_global16(dst + c * 8, lds128(reinterpret_cast<const float4*>(sl + c * 16)));
       }
     } else {
-      const int h = it.oc * 8 + g8;
+      const int h = oc * 8 + g8;
       uint32_t x[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -447,7 +449,7 @@ __global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams 
       }
       const dd r = head_rrms4(x, is_txt ? P.txt.eps : P.img.eps);
       const f2 rh = f2_make(r.hi, r.hi), rl = f2_make(r.lo, r.lo);
-      const uint8_t* wv = wsm + ((is_txt ? 0 : 2) + it.type) * 256 + qtr * 16;
+      const uint8_t* wv = wsm + ((is_txt ? 0 : 2) + type) * 256 + qtr * 16;
       uint32_t n[16];
       bool unsure = false;
 #pragma unroll
@@ -482,7 +484,7 @@ __global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams 
         o[4 * j + 3] = rope_word(n[4 * j + 3], c4.w, s4.w);
       }
       if (h < H) {
-        uint16_t* dst = (it.type == 0 ? P.jq : P.jk) + it.token * row_len + h * kHeadDim + qtr * 32;
+        uint16_t* dst = (type == 0 ? P.jq : P.jk) + it.token * row_len + h * kHeadDim + qtr * 32;
         st_stream32(dst, *reinterpret_cast<const uint32_t(*)[8]>(o));
         st_stream32(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(o + 8));
       }
