@@ -51,6 +51,14 @@ __device__ __forceinline__ void wait_for_producers() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Lets the next kernel in the stream (launched with programmatic serialization) be scheduled
+// onto SMs this grid frees; it still waits in griddepcontrol.wait for this grid to complete.
+// Only for persistent grids whose CTAs are all resident from the start, so waiting dependents
+// never hold resources one of our own CTAs still needs.
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Streaming 16-byte global accesses (data touched once).
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }

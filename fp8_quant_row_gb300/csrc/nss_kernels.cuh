@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
   const RowBlock blk = cta_rows(p.rows, p.mod_rows, n_mod, blockIdx.x, gridDim.x);
   if (blk.begin >= blk.end) return;  // uniform across the CTA
   wait_for_producers();
+  allow_dependents();
   unsigned char* my_ring = ring + size_t(warp) * kStages * L::kStageBytes;
 
   // Row r's part for this warp -> ring stage (each lane copies exactly the chunks it reads).

@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams 
   uint8_t* wsm = qkv_smem;
   uint8_t* ring = qkv_smem + 1024 + warp * (kQkvDepth * kQkvSlotBytes);
   wait_for_producers();
+  allow_dependents();
 
   if (tid < 64) {  // the four weight vectors, planar (a stream without tokens has none)
     const int w = tid >> 4, c = tid & 15;
