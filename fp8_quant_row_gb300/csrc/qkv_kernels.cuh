@@ -313,15 +313,13 @@ __device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], float eps) {
 }
 
 // Normalised words n = RN_bf16(x w r) for one packed word; sets `unsure` when the fast value
-// could round the other way (the bracket t (1 +- 2^-20), wider than the fast path's error,
-// rounds to two different BF16 pairs).
+// could round the other way (its low 16 bits lie within 8 of the BF16 midpoint pattern; the
+// fast path is within one fp32 ulp of the exact value).
 __device__ __forceinline__ uint32_t norm_word(uint32_t xw, uint32_t ww, f2 rh, f2 rl,
                                               bool& unsure) {
   const f2 p = mul2(bf2_to_f2(xw), bf2_to_f2(ww));  // exact
   const f2 t = fma2(p, rh, mul2(p, rl));
-  const f2 up = fma2(t, f2_make(0x1p-20f, 0x1p-20f), t);
-  const f2 dn = fma2(t, f2_make(-0x1p-20f, -0x1p-20f), t);
-  unsure |= pack_bf16x2(f2_lo(up), f2_hi(up)) != pack_bf16x2(f2_lo(dn), f2_hi(dn));
+  unsure |= near_bf16_midpoint(f2_lo(t)) | near_bf16_midpoint(f2_hi(t));
   return pack_bf16x2(f2_lo(t), f2_hi(t));
 }
 
