@@ -422,41 +422,58 @@ def time_case(torch, case: Case, steps: int, warmup: int, use_graph=True, barrie
 
 
 def e2e_measure(torch, lib, case: Case, steps: int):
-    """Same metric through the C ABI with host buffers: per step, pinned host x -> device,
-    kernel, device y and q -> pinned host, all on one stream inside the timed region."""
+    """Same metric through the C ABI with host buffers. Every step copies its x from pinned
+    host memory to the device, runs the kernel and copies y and q back to pinned host memory.
+    Steps alternate between two streams with their own device and host buffers, so step i+1's
+    host-to-device copy overlaps step i's device-to-host copy (both copy directions run at
+    once); the timed region spans all K steps on both streams (CUDA events)."""
     xs, ys, qs, sc, sh, s, inp = case.keep
     R, C = inp["x"].shape
     import numpy as np
     hx = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    hy = torch.empty(R, C, dtype=torch.bfloat16).pin_memory()
-    hq = torch.empty(R, C, dtype=torch.uint8).pin_memory()
-    dx, dy, dq = xs[0], ys[0], qs[0]
-    stream = torch.cuda.current_stream()
+    nb = 2
+    hy = [torch.empty(R, C, dtype=torch.bfloat16).pin_memory() for _ in range(nb)]
+    hq = [torch.empty(R, C, dtype=torch.uint8).pin_memory() for _ in range(nb)]
+    dx, dy, dq = xs[:nb], ys[:nb], qs[:nb]
+    streams = [torch.cuda.Stream() for _ in range(nb)]
 
-    def step():
-        dx.copy_(hx, non_blocking=True)
-        st = lib.fp8q_nss_fp8(dy.data_ptr(), dq.data_ptr(), dx.data_ptr(), sc.data_ptr(),
-                              sh.data_ptr(), 0, s.data_ptr(), R, C, 1e-6, stream.cuda_stream)
-        if st:
-            raise RuntimeError(f"status {st}")
-        hy.copy_(dy, non_blocking=True)
-        hq.copy_(dq, non_blocking=True)
+    def step(i):
+        b = i % nb
+        st = streams[b]
+        with torch.cuda.stream(st):
+            dx[b].copy_(hx, non_blocking=True)
+            status = lib.fp8q_nss_fp8(dy[b].data_ptr(), dq[b].data_ptr(), dx[b].data_ptr(),
+                                      sc.data_ptr(), sh.data_ptr(), 0, s.data_ptr(), R, C, 1e-6,
+                                      st.cuda_stream)
+            if status:
+                raise RuntimeError(f"status {status}")
+            hy[b].copy_(dy[b], non_blocking=True)
+            hq[b].copy_(dq[b], non_blocking=True)
 
-    for _ in range(3):
-        step()
+    for i in range(3):
+        step(i)
     torch.cuda.synchronize()
+    main = torch.cuda.current_stream()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    for _ in range(steps):
-        step()
-    ev1.record()
+    ev0.record(main)
+    for st in streams:
+        st.wait_event(ev0)
+    for i in range(steps):
+        step(i)
+    for st in streams:
+        done = torch.cuda.Event()
+        done.record(st)
+        main.wait_event(done)
+    ev1.record(main)
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
     return {"value": R * steps / (ms / 1e3), "unit": "rows/s", "steps": steps,
             "ms_per_step": ms / steps, "h2d_bytes_per_step": R * C * 2,
-            "d2h_bytes_per_step": R * C * 3, "method": "pinned host buffers, torch copies + "
-            "C-ABI launch on one stream, CUDA events"}
+            "d2h_bytes_per_step": R * C * 3,
+            "method": "pinned host buffers; torch copies + C-ABI launch; steps alternate between "
+                      "two streams (double-buffered), so one step's H2D overlaps the previous "
+                      "step's D2H; CUDA events around all steps"}
 
 
 def cpu_baseline(sample_seconds: float = 10.0):
