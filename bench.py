@@ -476,6 +476,22 @@ def e2e_measure(torch, lib, case: Case, steps: int):
                       "step's D2H; CUDA events around all steps"}
 
 
+def host_cpu() -> str:
+    """The host's CPU model and logical core count (lscpu where available)."""
+    import platform
+    import subprocess
+    model = platform.processor() or platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return f"{model}, {os.cpu_count()} logical cores, {platform.machine()}"
+
+
 def cpu_baseline(sample_seconds: float = 10.0):
     """The oracle as it stands, single-threaded, on row chunks of the main workload."""
     import numpy as np
@@ -492,6 +508,7 @@ def cpu_baseline(sample_seconds: float = 10.0):
         if el >= sample_seconds:
             break
     return {"value": rows_done / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "host": host_cpu(),
             "sample": f"{rows_done} rows of the nss_fp8 Qwen-Image workload (256-row chunks, "
                       f"{el:.1f} s, single-threaded C oracle, fp64 statistics)"}
 
@@ -635,6 +652,7 @@ def run_reference(args):
                                f"{c['input_scale']}; each step a {rows_per_step}-row sample",
                    "rows_per_step": rows_per_step},
         "cpu_baseline": {"value": round(value, 2), "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "host": host_cpu(),
                          "sample": f"{rows_per_step} rows per step x {args.steps} steps"},
         "e2e": {"value": round(value, 2), "unit": "rows/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

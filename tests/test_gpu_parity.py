@@ -478,3 +478,53 @@ def test_runs_on_a_side_stream_and_is_deterministic():
     torch.cuda.synchronize()
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
     assert torch.equal(q1.view(torch.uint8), q2.view(torch.uint8))
+
+
+def test_calls_capture_into_a_cuda_graph_and_replay():
+    """Every entry point is asynchronous on the given stream and allocates nothing, so it can
+    be captured into a CUDA graph; replays on new inputs (copied into the captured buffers)
+    must equal direct calls."""
+    lib = fq()
+    rng_inputs = [W.config_inputs("nss_qwen", rows=256, seed=s) for s in (11, 12)]
+    x = G.dev_bf16(rng_inputs[0]["x"])
+    sc, sh = G.dev_bf16(rng_inputs[0]["scale"]), G.dev_bf16(rng_inputs[0]["shift"])
+    s = G.dev_scale(0.25)
+    y = torch.empty_like(x)
+    q = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device="cuda")
+    t = W.token_cat_inputs(128, 6144, 18432, seed=5)
+    a, m = G.dev_bf16(t["a"]), G.dev_bf16(t["m"])
+    g = G.dev_scale(60.0)
+    q4 = torch.empty(128, 12288, dtype=torch.uint8, device="cuda")
+    sf = torch.empty(lib.nvfp4_scale_bytes(128, 24576), dtype=torch.uint8, device="cuda")
+    d = W.qkv_inputs(8, 32, 24, seed=6)
+    txt, img = _dev_stream(d["txt"], 24), _dev_stream(d["img"], 24)
+    jo = tuple(torch.empty(40, 24, 128, dtype=torch.bfloat16, device="cuda") for _ in range(3))
+
+    def calls():
+        lib.nss_fp8(x, sc, sh, s, y=y, q=q)
+        lib.token_cat_nvfp4(a, m, g, q=q4, sf=sf)
+        lib.qkv_epilogue(txt, img, 24, out=jo)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        calls()  # warm-up outside capture (occupancy queries, attributes)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        calls()
+    # new inputs into the captured buffers, replay, compare with direct calls
+    x.copy_(G.dev_bf16(rng_inputs[1]["x"]))
+    a.copy_(G.dev_bf16(W.token_cat_inputs(128, 6144, 18432, seed=7)["a"]))
+    graph.replay()
+    torch.cuda.synchronize()
+    got = [G.host_u16(y), G.host_u8(q), G.host_u8(q4), G.host_u8(sf)] + [G.host_u16(o) for o in jo]
+    y2, q2 = lib.nss_fp8(x, sc, sh, s)
+    q42, sf2 = lib.token_cat_nvfp4(a, m, g)
+    jo2 = lib.qkv_epilogue(txt, img, 24)
+    torch.cuda.synchronize()
+    want = [G.host_u16(y2), G.host_u8(q2), G.host_u8(q42), G.host_u8(sf2)] + [G.host_u16(o) for o in jo2]
+    for i, (u, v) in enumerate(zip(got, want)):
+        assert np.array_equal(u, v), i
+    assert not np.array_equal(got[0], G.host_u16(G.dev_bf16(rng_inputs[0]["x"])))  # really replayed
