@@ -9,10 +9,10 @@
 //   V:     copied,
 // written to joint [text tokens + image tokens, heads, 128] buffers, text first.
 //
-// Layout: one CTA per joint token (grid-stride), 6 warps: two per kind (Q, K, V). A warp takes
-// four heads at a time; 8 lanes per head, 16 consecutive values (one 32-byte load) per lane,
-// so each lane's 8 packed BF16 words are exactly its 8 RoPE pairs. A Q/K warp loads all its
-// heads of the token before computing any.
+// Two kernels: qkv_ring_kernel (up to 64 heads; per-warp cp.async pipelines, four lanes per
+// head, described below) and qkv_epilogue_kernel (any head count: one CTA per joint token,
+// 6 warps, two per kind; 8 lanes per head with one 32-byte load each, so a lane's 8 packed BF16
+// words are exactly its 8 RoPE pairs; a Q/K warp loads all its heads before computing any).
 //
 // Exactness of n: sum(x^2) per head is formed without rounding error that matters. Squares
 // of BF16 values are exact in fp32. They are accumulated from an offset K2 = 2^(2E+9) >= 128
@@ -21,7 +21,7 @@
 // error; the e are added to a second offset accumulator 48u (one binade, ulp u 2^-18) with
 // the FastTwoSum error kept, and those second-level errors summed in fp32 (their rounding is
 // ~2^-53 of the total). Accumulator offsets come off as exact integers of their ulps, which
-// the 8 lanes of a head add as integers. 1/sqrt(mean + eps) is a double-float (~2^-45). The
+// the lanes of a head add as integers. 1/sqrt(mean + eps) is a double-float (~2^-45). The
 // fast path t = fma(p, r_hi, p r_lo), p = x w (exact), is within one fp32 ulp of the exact
 // value; only values whose low 16 bits lie within 8 of the BF16 midpoint pattern take the
 // exact path (TwoProduct + the tie broken by the low part).
@@ -253,15 +253,6 @@ __device__ __forceinline__ void lds_words4(const uint8_t* p, uint32_t* w) {
   w[1] = __float_as_uint(v.y);
   w[2] = __float_as_uint(v.z);
   w[3] = __float_as_uint(v.w);
-}
-
-__device__ __forceinline__ void cp_async_wait_dyn(int pending) {
-  switch (pending) {
-    case 0: cp_async_wait<0>(); break;
-    case 1: cp_async_wait<1>(); break;
-    case 2: cp_async_wait<2>(); break;
-    default: cp_async_wait<3>(); break;
-  }
 }
 
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {

@@ -14,8 +14,7 @@ def pytest_configure(config):
 
 
 # Mismatch counts of the one-ulp parity checks (LayerNorm y, QKV-epilogue q and k: elements
-# that differ from the oracle by
-# one bf16 ulp), reported at the end of the run.
+# that differ from the oracle by one bf16 ulp), reported at the end of the run.
 PARITY_COUNTS = []
 
 
