@@ -151,6 +151,32 @@ def test_bf16_from_f32_matches_torch_on_all_low_halves():
         assert np.all((ours[nan] & 0x7F80) == 0x7F80) and np.all((ours[nan] & 0x7F) != 0)
 
 
+@pytest.mark.slow
+def test_bf16_from_f32_exhaustive_against_torch():
+    """Every one of the 2^32 fp32 bit patterns (NaNs: still NaN)."""
+    low = np.arange(0x10000, dtype=np.uint32)
+    for h0 in range(0, 0x10000, 0x200):
+        highs = np.arange(h0, h0 + 0x200, dtype=np.uint32)
+        f = ((highs[:, None] << 16) | low[None, :]).ravel().view(np.float32)
+        ours = oracle.bf16_from_f32_array(f)
+        ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        nan = np.isnan(f)
+        assert np.array_equal(ours[~nan], ref[~nan]), hex(h0)
+        assert np.all((ours[nan] & 0x7F80) == 0x7F80) and np.all((ours[nan] & 0x7F) != 0)
+
+
+@pytest.mark.slow
+def test_e4m3_encode_exhaustive_against_torch():
+    """Every finite fp32 bit pattern: clamp to +-448 and cast with torch, vs the oracle."""
+    low = np.arange(0x10000, dtype=np.uint32)
+    for h0 in range(0, 0x10000, 0x200):
+        highs = np.arange(h0, h0 + 0x200, dtype=np.uint32)
+        f = ((highs[:, None] << 16) | low[None, :]).ravel().view(np.float32)
+        f = f[np.isfinite(f)]
+        ours = oracle.e4m3_encode_array(f)
+        assert np.array_equal(ours, _torch_satfinite_e4m3(f)), hex(h0)
+
+
 def test_bf16_from_f64_matches_exact_nearest_search():
     rng = np.random.default_rng(5)
     vals = list(rng.standard_normal(3000) * 2.0 ** rng.integers(-140, 128, 3000))
