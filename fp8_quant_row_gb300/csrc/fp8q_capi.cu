@@ -506,7 +506,7 @@ const char* fp8q_status_string(int status) {
   switch (status) {
     case FP8Q_OK: return "ok";
     case FP8Q_ERR_NULL: return "null pointer";
-    case FP8Q_ERR_ALIGN: return "pointer not aligned (16 bytes; 32 for NVFP4 data)";
+    case FP8Q_ERR_ALIGN: return "pointer not aligned (16 bytes; 32 for NVFP4 and QKV data)";
     case FP8Q_ERR_SHAPE: return "unsupported shape";
     case FP8Q_ERR_UNSUPPORTED: return "device is not compute capability 10.3 (GB300)";
     case FP8Q_ERR_ALIAS: return "an output overlaps an input or another output";
@@ -520,6 +520,6 @@ int fp8q_last_cuda_error(void) { return g_last_cuda_error; }
 
 const char* fp8q_last_error_detail(void) { return g_last_detail; }
 
-int fp8q_version(void) { return 0x000100; }
+int fp8q_version(void) { return 0x000200; }
 
 }  // extern "C"

@@ -64,7 +64,7 @@ extern "C" {
 typedef enum fp8q_status {
     FP8Q_OK = 0,
     FP8Q_ERR_NULL = 1,        /* a required pointer is NULL (with rows > 0)                   */
-    FP8Q_ERR_ALIGN = 2,       /* a tensor pointer is not 16-byte aligned                      */
+    FP8Q_ERR_ALIGN = 2,       /* a tensor pointer is not 16-byte aligned (32 where stated)    */
     FP8Q_ERR_SHAPE = 3,       /* rows < 0, unsupported cols / a_cols / m_cols, mod_rows < 0   */
     FP8Q_ERR_UNSUPPORTED = 4, /* current device is not compute capability 10.3                */
     FP8Q_ERR_ALIAS = 5,       /* an output overlaps an input or another output (see per call) */
@@ -234,7 +234,7 @@ int fp8q_last_cuda_error(void);
  * (thread-local static string, "" if none; overwritten by the next failure). */
 const char* fp8q_last_error_detail(void);
 
-/* Library ABI version: 0x00MMmmpp. */
+/* Library ABI version: 0x00MMmmpp (0.2.0: token_cat_nvfp4 and qkv_epilogue added). */
 int fp8q_version(void);
 
 #ifdef __cplusplus
