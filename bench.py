@@ -251,6 +251,32 @@ def extra_cases(torch, lib, l2, only=None):
         case.keep = (bufs, b, g)
         return case
 
+    def nss_tiny():
+        c = W.CONFIGS["nss_tiny"]
+        inp = W.config_inputs("nss_tiny")
+        R, C = inp["x"].shape
+        per = R * C * 5
+        n = n_sets_for(per, l2)
+        bufs = [dict(x=dev_bf16(torch, inp["x"]),
+                     y=torch.empty(R, C, dtype=torch.bfloat16, device="cuda"),
+                     q=torch.empty(R, C, dtype=torch.uint8, device="cuda")) for _ in range(n)]
+        sc, shf = dev_bf16(torch, inp["scale"]), dev_bf16(torch, inp["shift"])
+        s = torch.tensor([c["input_scale"]], dtype=torch.float32, device="cuda")
+
+        def nt(i):
+            d = bufs[i % len(bufs)]
+            st = lib.fp8q_nss_fp8(d["y"].data_ptr(), d["q"].data_ptr(), d["x"].data_ptr(),
+                                  sc.data_ptr(), shf.data_ptr(), 0, s.data_ptr(), R, C, 1e-6,
+                                  sh_())
+            if st:
+                raise RuntimeError(f"nss tiny status {st}")
+
+        case = Case("nss_fp8", nt, n, per, R, "nss_fp8_tiny",
+                    f"x bf16 [{R},{C}], latency-bound ({R} rows over all SMs); {n} rotating "
+                    f"buffer sets keep the inputs cold")
+        case.keep = (bufs, sc, shf, s)
+        return case
+
     def nss_flux():
         c = W.CONFIGS["nss_flux"]
         inp = W.config_inputs("nss_flux")
@@ -369,7 +395,8 @@ def extra_cases(torch, lib, l2, only=None):
         case.keep = sets
         return case
 
-    builders = {"scale_residual_qwen": scale_residual_qwen, "bias_mul_add_qwen": bias_mul_add_qwen,
+    builders = {"nss_tiny": nss_tiny,
+                "scale_residual_qwen": scale_residual_qwen, "bias_mul_add_qwen": bias_mul_add_qwen,
                 "nss_flux": nss_flux, "token_cat_flux": token_cat_flux,
                 "token_cat_nvfp4_flux": token_cat_nvfp4_flux, "qkv_qwen": qkv_qwen}
     return {k: f for k, f in builders.items() if only is None or k == only}
@@ -689,7 +716,7 @@ def main():
     ap.add_argument("--skip-kernels", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--profile-only", choices=("nss_qwen", "scale_residual_qwen",
+    ap.add_argument("--profile-only", choices=("nss_qwen", "nss_tiny", "scale_residual_qwen",
                                                "token_cat_nvfp4_flux", "qkv_qwen",
                                                "bias_mul_add_qwen", "nss_flux", "token_cat_flux"),
                     help="only launch this workload (W+K launches, no timing): for ncu captures")
