@@ -326,9 +326,9 @@ def extra_cases(torch, lib, l2, only=None):
         case.keep = (bufs, s)
         return case
 
-    def token_cat_nvfp4_flux():
+    def token_cat_nvfp4_flux(rows=None):
         c = W.CONFIGS["token_cat_nvfp4_flux"]
-        inp = W.config_inputs("token_cat_nvfp4_flux")
+        inp = W.config_inputs("token_cat_nvfp4_flux", rows=rows)
         R, A = inp["a"].shape
         M = inp["m"].shape[1]
         K = (A + M) // 16
@@ -349,17 +349,18 @@ def extra_cases(torch, lib, l2, only=None):
             if st:
                 raise RuntimeError(f"token_cat_nvfp4 status {st}")
 
-        case = Case("token_cat_nvfp4", tc4, n, per, R, "token_cat_nvfp4_flux",
+        case = Case("token_cat_nvfp4", tc4, n, per, R,
+                    "token_cat_nvfp4_flux" if rows is None else f"token_cat_nvfp4_flux_{rows}",
                     f"a bf16 [{R},{A}] + m bf16 [{R},{M}] -> q e2m1 [{R},{(A + M) // 2}] "
                     f"bytes + {K} e4m3 block scales per row (128x4 tiles), global scale "
                     f"{c['global_scale']}")
         case.keep = (bufs, s)
         return case
 
-    def qkv_qwen():
+    def qkv(name):
         import fp8_quant_row_gb300._capi as capi
-        c = W.CONFIGS["qkv_qwen"]
-        d = W.config_inputs("qkv_qwen")
+        c = W.CONFIGS[name]
+        d = W.config_inputs(name)
         H = c["heads"]
         T = c["txt_tokens"] + c["img_tokens"]
         per = T * (3 * H * 128 * 2 * 2 + 128 * 4)
@@ -381,14 +382,14 @@ def extra_cases(torch, lib, l2, only=None):
             outs = [torch.empty(T, H, 128, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
             sets.append((streams, outs, keep))
 
-        def qkv(i):
+        def run_qkv(i):
             streams, outs, _ = sets[i % len(sets)]
             st = lib.fp8q_qkv_epilogue(outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(),
                                        streams[0], streams[1], H, sh_())
             if st:
                 raise RuntimeError(f"qkv_epilogue status {st}")
 
-        case = Case("qkv_epilogue", qkv, n, per, T, "qkv_epilogue_qwen",
+        case = Case("qkv_epilogue", run_qkv, n, per, T, f"qkv_epilogue_{name[4:]}",
                     f"packed QKV bf16 text [{c['txt_tokens']},{3 * H * 128}] + image "
                     f"[{c['img_tokens']},{3 * H * 128}], {H} heads x 128 -> joint q, k, v "
                     f"[{T},{H},128] (RMSNorm + interleaved RoPE on q, k)")
@@ -398,7 +399,12 @@ def extra_cases(torch, lib, l2, only=None):
     builders = {"nss_tiny": nss_tiny,
                 "scale_residual_qwen": scale_residual_qwen, "bias_mul_add_qwen": bias_mul_add_qwen,
                 "nss_flux": nss_flux, "token_cat_flux": token_cat_flux,
-                "token_cat_nvfp4_flux": token_cat_nvfp4_flux, "qkv_qwen": qkv_qwen}
+                "token_cat_nvfp4_flux": token_cat_nvfp4_flux,
+                # the pages' token-cat microbenchmark token counts (latency end)
+                "token_cat_nvfp4_flux_17": lambda: token_cat_nvfp4_flux(17),
+                "token_cat_nvfp4_flux_512": lambda: token_cat_nvfp4_flux(512),
+                "token_cat_nvfp4_flux_4096": lambda: token_cat_nvfp4_flux(4096),
+                "qkv_qwen": lambda: qkv("qkv_qwen"), "qkv_flux": lambda: qkv("qkv_flux")}
     return {k: f for k, f in builders.items() if only is None or k == only}
 
 
@@ -717,7 +723,7 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile-only", choices=("nss_qwen", "nss_tiny", "scale_residual_qwen",
-                                               "token_cat_nvfp4_flux", "qkv_qwen",
+                                               "token_cat_nvfp4_flux", "qkv_qwen", "qkv_flux",
                                                "bias_mul_add_qwen", "nss_flux", "token_cat_flux"),
                     help="only launch this workload (W+K launches, no timing): for ncu captures")
     args = ap.parse_args()
