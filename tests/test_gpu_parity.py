@@ -322,6 +322,14 @@ def test_token_cat_nvfp4_shapes_and_padding(rows, a_cols, m_cols):
         check_nvfp4(inp["a"], inp["m"], g, f"{rows}x{a_cols}+{m_cols} g={g}")
 
 
+def test_token_cat_nvfp4_more_row_groups_than_one_grid_dimension():
+    """600,000 rows = 75,000 eight-row groups: more than the 65,535 a grid dimension holds, so
+    the kernel's row-group loop strides (the pages' wrapper stops at 65,408 rows)."""
+    rows = 600_000
+    inp = W.token_cat_inputs(rows, 64, 64, seed=9)
+    check_nvfp4(inp["a"], inp["m"], 60.0, "600k rows")
+
+
 def test_token_cat_nvfp4_special_values_and_ties():
     """Exact E2M1 midpoints (ties to even), signed zeros, +-Inf, bf16 subnormals and the
     largest finite bf16, block scales that saturate or vanish."""
