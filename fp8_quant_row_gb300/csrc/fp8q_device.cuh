@@ -302,6 +302,14 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Lane-wise max(|a|, |b|) of two bf16 pairs (sign = xor of the signs, not used): the
+// magnitude bits of the result are the larger magnitude of each lane, in one instruction.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // Knuth TwoSum on both lanes: s + e == a + b exactly.
 __device__ __forceinline__ void two_sum2(f2 a, f2 b, f2& s, f2& e) {
   s = add2(a, b);

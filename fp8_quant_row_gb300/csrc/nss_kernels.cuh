@@ -438,15 +438,15 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
     // (K >= 256 max|x|, K2 >= 128 max x^2 over the warp's part of the row), so every addition
     // satisfies FastTwoSum's exponent condition and its rounding error is exact; the errors
     // are accumulated separately. v*v is exact (8-bit significands). max|x| comes from a
-    // packed max over the raw bf16 magnitudes, reduced over the warp.
+    // packed bf16 abs-max (max.xorsign.abs.bf16x2) over the row part, reduced over the warp.
     uint32_t m2 = 0;
 #pragma unroll 4
     for (int j = 0; j < V; ++j) {
       const uint4 xv = stage[j * 32];
-      m2 = max_u16x2(m2, max_u16x2(xv.x & 0x7FFF7FFFu, xv.y & 0x7FFF7FFFu));
-      m2 = max_u16x2(m2, max_u16x2(xv.z & 0x7FFF7FFFu, xv.w & 0x7FFF7FFFu));
+      m2 = absmax_bf16x2(m2, absmax_bf16x2(absmax_bf16x2(xv.x, xv.y), absmax_bf16x2(xv.z, xv.w)));
     }
-    const uint32_t mexp = __reduce_max_sync(0xffffffffu, (max(m2 & 0xFFFFu, m2 >> 16) >> 7) & 0xFFu);
+    const uint32_t mexp =
+        __reduce_max_sync(0xffffffffu, (max(m2 & 0x7FFFu, (m2 >> 16) & 0x7FFFu) >> 7) & 0xFFu);
     const RowOffsets off = row_offsets(mexp);
     f2 sx = f2_make(off.K, off.K), sq = f2_make(off.K2, off.K2), ex = f2_make(0.0f, 0.0f),
        eq = ex;

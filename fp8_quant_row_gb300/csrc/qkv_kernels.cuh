@@ -255,12 +255,6 @@ __device__ __forceinline__ void lds_words4(const uint8_t* p, uint32_t* w) {
   w[3] = __float_as_uint(v.w);
 }
 
-__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 // 1 / sqrt(sum(x^2) / 128 + eps) for the head held by this lane's group of 4 lanes (32 values
 // each), with the same exact accumulation as head_rrms.
 __device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], float eps) {
