@@ -492,7 +492,8 @@ fp8q_status fp8q_qkv_epilogue(void* joint_q, void* joint_k, void* joint_v,
   p.heads = int(heads);
   if (heads <= fp8q::kQkvRingMaxHeads) {
     // per-warp item pipelines; two or more CTAs per SM
-    const size_t smem = 1024 + size_t(fp8q::kQkvRingWarps) * fp8q::kQkvDepth * fp8q::kQkvSlotBytes;
+    const size_t smem = fp8q::kQkvWeightBytes +
+                        size_t(fp8q::kQkvRingWarps) * fp8q::kQkvDepth * fp8q::kQkvSlotBytes;
     auto* fn = fp8q::qkv_ring_kernel;
     int bps = 0;
     stt = blocks_per_sm(reinterpret_cast<const void*>(fn), fp8q::kQkvRingWarps * 32, smem, &bps);

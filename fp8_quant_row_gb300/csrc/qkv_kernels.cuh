@@ -300,17 +300,16 @@ __device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], float eps) {
 // Normalised words n = RN_bf16(x w r) for one packed word; sets `unsure` when the fast value
 // could round the other way (its low 16 bits lie within 8 of the BF16 midpoint pattern; the
 // fast path is within one fp32 ulp of the exact value).
-__device__ __forceinline__ uint32_t norm_word(uint32_t xw, uint32_t ww, f2 rh, f2 rl,
-                                              bool& unsure) {
-  const f2 p = mul2(bf2_to_f2(xw), bf2_to_f2(ww));  // exact
+__device__ __forceinline__ uint32_t norm_word(uint32_t xw, f2 wf, f2 rh, f2 rl, bool& unsure) {
+  const f2 p = mul2(bf2_to_f2(xw), wf);  // exact (BF16 x BF16 values)
   const f2 t = fma2(p, rh, mul2(p, rl));
   unsure |= near_bf16_midpoint(f2_lo(t)) | near_bf16_midpoint(f2_hi(t));
   return pack_bf16x2(f2_lo(t), f2_hi(t));
 }
 
-__device__ __noinline__ uint32_t norm_word_exact(uint32_t xw, uint32_t ww, float r_hi,
+__device__ __noinline__ uint32_t norm_word_exact(uint32_t xw, float w0, float w1, float r_hi,
                                                  float r_lo) {
-  const float p0 = __fmul_rn(bf_lo(xw), bf_lo(ww)), p1 = __fmul_rn(bf_hi(xw), bf_hi(ww));
+  const float p0 = __fmul_rn(bf_lo(xw), w0), p1 = __fmul_rn(bf_hi(xw), w1);
   return scaled_exact_bits(p0, r_hi, r_lo) | (scaled_exact_bits(p1, r_hi, r_lo) << 16);
 }
 
@@ -325,6 +324,7 @@ __device__ __forceinline__ uint32_t rope_word(uint32_t nw, float c, float s) {
 // eight-head blocks of Q, of K or of V. A Q/K item brings 2 KB of values (planar) and the
 // token's cos/sin row into the warp's slot; a V item brings 2 KB that go straight back out.
 constexpr int kQkvDepth = 4;           // slots per warp
+constexpr int kQkvWeightBytes = 2048;  // four fp32 RMSNorm weight vectors
 constexpr int kQkvSlotBytes = 2560;    // 8 heads x 256 B + cos/sin 512 B
 
 __global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams P) {
@@ -336,18 +336,23 @@ __global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams 
   const int per_token = 3 * octs;
   const int64_t row_len = int64_t(H) * kHeadDim;
   uint8_t* wsm = qkv_smem;
-  uint8_t* ring = qkv_smem + 1024 + warp * (kQkvDepth * kQkvSlotBytes);
+  uint8_t* ring = qkv_smem + kQkvWeightBytes + warp * (kQkvDepth * kQkvSlotBytes);
   wait_for_producers();
   allow_dependents();
 
-  if (tid < 64) {  // the four weight vectors, planar (a stream without tokens has none)
-    const int w = tid >> 4, c = tid & 15;
+  // The four weight vectors as fp32, planar: 16-byte chunk c (values 4c .. 4c+3) of the
+  // 32-value quarter q at c * 64 + q * 16 (a stream without tokens has none).
+  for (int t = tid; t < 4 * 64; t += kQkvRingWarps * 32) {
+    const int w = t >> 6, pi = t & 63;  // vector, value pair
     const uint16_t* src = w == 0 ? P.txt.wq : w == 1 ? P.txt.wk : w == 2 ? P.img.wq : P.img.wk;
     const bool present = (w < 2 ? P.txt.tokens : P.img.tokens) > 0;
-    if (present) cp_async16(wsm + w * 256 + (c & 3) * 64 + (c >> 2) * 16, src + c * 8);
+    if (present) {
+      const uint32_t pair = __ldg(reinterpret_cast<const uint32_t*>(src) + pi);
+      const int q = pi >> 4, ii = pi & 15;
+      *reinterpret_cast<float2*>(wsm + w * 512 + (ii >> 1) * 64 + q * 16 + (ii & 1) * 8) =
+          make_float2(bf_lo(pair), bf_hi(pair));
+    }
   }
-  cp_async_commit();
-  cp_async_wait<0>();
   __syncthreads();
 
   // Items gw, gw + W, gw + 2W, ... as (token, remainder) pairs, advanced without division.
@@ -433,27 +438,24 @@ __global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams 
       }
       const dd r = head_rrms4(x, is_txt ? P.txt.eps : P.img.eps);
       const f2 rh = f2_make(r.hi, r.hi), rl = f2_make(r.lo, r.lo);
-      const uint8_t* wv = wsm + ((is_txt ? 0 : 2) + type) * 256 + qtr * 16;
+      const uint8_t* wv = wsm + ((is_txt ? 0 : 2) + type) * 512 + qtr * 16;
       uint32_t n[16];
       bool unsure = false;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t wt[4];
-        lds_words4(wv + j * 64, wt);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) n[4 * j + i] = norm_word(x[4 * j + i], wt[i], rh, rl, unsure);
+      for (int c = 0; c < 8; ++c) {  // chunk c: value pairs 2c, 2c + 1 of this lane
+        const float4 w4 = lds128(reinterpret_cast<const float4*>(wv + c * 64));
+        n[2 * c] = norm_word(x[2 * c], f2_make(w4.x, w4.y), rh, rl, unsure);
+        n[2 * c + 1] = norm_word(x[2 * c + 1], f2_make(w4.z, w4.w), rh, rl, unsure);
       }
-      if (unsure) {  // rare: redo the words whose bracket straddles a rounding boundary
+      if (unsure) {  // rare: redo the words whose fast value may round the other way
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t wt[4];
-          lds_words4(wv + j * 64, wt);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            bool u1 = false;
-            norm_word(x[4 * j + i], wt[i], rh, rl, u1);
-            if (u1) n[4 * j + i] = norm_word_exact(x[4 * j + i], wt[i], r.hi, r.lo);
-          }
+        for (int c = 0; c < 8; ++c) {
+          const float4 w4 = lds128(reinterpret_cast<const float4*>(wv + c * 64));
+          bool u0 = false, u1 = false;
+          norm_word(x[2 * c], f2_make(w4.x, w4.y), rh, rl, u0);
+          norm_word(x[2 * c + 1], f2_make(w4.z, w4.w), rh, rl, u1);
+          if (u0) n[2 * c] = norm_word_exact(x[2 * c], w4.x, w4.y, r.hi, r.lo);
+          if (u1) n[2 * c + 1] = norm_word_exact(x[2 * c + 1], w4.z, w4.w, r.hi, r.lo);
         }
       }
       const uint8_t* csv = sl + 2048 + qtr * 16;
