@@ -256,8 +256,10 @@ __device__ __forceinline__ void lds_words4(const uint8_t* p, uint32_t* w) {
 }
 
 // 1 / sqrt(sum(x^2) / 128 + eps) for the head held by this lane's group of 4 lanes (32 values
-// each), with the same exact accumulation as head_rrms.
-__device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], float eps) {
+// each), with the same exact accumulation as head_rrms; also returns p = x * weight (exact),
+// the weight pairs read as fp32 from shared memory, so each value is unpacked once.
+__device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], const uint8_t* wv, float eps,
+                                         f2 (&p)[16]) {
   uint32_t m = absmax_bf16x2(w[0], w[1]);
 #pragma unroll
   for (int i = 2; i < 16; ++i) m = absmax_bf16x2(m, w[i]);
@@ -271,6 +273,11 @@ __device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], float eps) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const f2 v = bf2_to_f2(w[i]);
+    if ((i & 1) == 0) {
+      const float4 w4 = lds128(reinterpret_cast<const float4*>(wv + (i >> 1) * 64));
+      p[i] = mul2(v, f2_make(w4.x, w4.y));
+      p[i + 1] = mul2(bf2_to_f2(w[i + 1]), f2_make(w4.z, w4.w));
+    }
     const f2 sn = fma2(v, v, S);
     const f2 e = fma2(v, v, sub2(S, sn));  // exact error of sn
     S = sn;
@@ -300,16 +307,13 @@ __device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], float eps) {
 // Normalised words n = RN_bf16(x w r) for one packed word; sets `unsure` when the fast value
 // could round the other way (its low 16 bits lie within 8 of the BF16 midpoint pattern; the
 // fast path is within one fp32 ulp of the exact value).
-__device__ __forceinline__ uint32_t norm_word(uint32_t xw, f2 wf, f2 rh, f2 rl, bool& unsure) {
-  const f2 p = mul2(bf2_to_f2(xw), wf);  // exact (BF16 x BF16 values)
+__device__ __forceinline__ uint32_t norm_word(f2 p, f2 rh, f2 rl, bool& unsure) {
   const f2 t = fma2(p, rh, mul2(p, rl));
   unsure |= near_bf16_midpoint(f2_lo(t)) | near_bf16_midpoint(f2_hi(t));
   return pack_bf16x2(f2_lo(t), f2_hi(t));
 }
 
-__device__ __noinline__ uint32_t norm_word_exact(uint32_t xw, float w0, float w1, float r_hi,
-                                                 float r_lo) {
-  const float p0 = __fmul_rn(bf_lo(xw), w0), p1 = __fmul_rn(bf_hi(xw), w1);
+__device__ __noinline__ uint32_t norm_word_exact(float p0, float p1, float r_hi, float r_lo) {
   return scaled_exact_bits(p0, r_hi, r_lo) | (scaled_exact_bits(p1, r_hi, r_lo) << 16);
 }
 
@@ -436,26 +440,20 @@ __global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams 
           x[4 * j] = x[4 * j + 1] = x[4 * j + 2] = x[4 * j + 3] = 0u;
         }
       }
-      const dd r = head_rrms4(x, is_txt ? P.txt.eps : P.img.eps);
-      const f2 rh = f2_make(r.hi, r.hi), rl = f2_make(r.lo, r.lo);
       const uint8_t* wv = wsm + ((is_txt ? 0 : 2) + type) * 512 + qtr * 16;
+      f2 p[16];
+      const dd r = head_rrms4(x, wv, is_txt ? P.txt.eps : P.img.eps, p);
+      const f2 rh = f2_make(r.hi, r.hi), rl = f2_make(r.lo, r.lo);
       uint32_t n[16];
       bool unsure = false;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {  // chunk c: value pairs 2c, 2c + 1 of this lane
-        const float4 w4 = lds128(reinterpret_cast<const float4*>(wv + c * 64));
-        n[2 * c] = norm_word(x[2 * c], f2_make(w4.x, w4.y), rh, rl, unsure);
-        n[2 * c + 1] = norm_word(x[2 * c + 1], f2_make(w4.z, w4.w), rh, rl, unsure);
-      }
+      for (int i = 0; i < 16; ++i) n[i] = norm_word(p[i], rh, rl, unsure);
       if (unsure) {  // rare: redo the words whose fast value may round the other way
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 w4 = lds128(reinterpret_cast<const float4*>(wv + c * 64));
-          bool u0 = false, u1 = false;
-          norm_word(x[2 * c], f2_make(w4.x, w4.y), rh, rl, u0);
-          norm_word(x[2 * c + 1], f2_make(w4.z, w4.w), rh, rl, u1);
-          if (u0) n[2 * c] = norm_word_exact(x[2 * c], w4.x, w4.y, r.hi, r.lo);
-          if (u1) n[2 * c + 1] = norm_word_exact(x[2 * c + 1], w4.z, w4.w, r.hi, r.lo);
+        for (int i = 0; i < 16; ++i) {
+          bool u = false;
+          norm_word(p[i], rh, rl, u);
+          if (u) n[i] = norm_word_exact(f2_lo(p[i]), f2_hi(p[i]), r.hi, r.lo);
         }
       }
       const uint8_t* csv = sl + 2048 + qtr * 16;
