@@ -68,13 +68,13 @@ __device__ __forceinline__ uint32_t pack_e2m1x8(f2 p0, f2 p1, f2 p2, f2 p3) {
   return r;
 }
 
-// max |x| of a 16-element group held as eight bf16x2 words, as an fp32 value. |bf16| bit
-// patterns order like their values, so the maximum is an integer max of the magnitudes.
+// max |x| of a 16-element group held as eight bf16x2 words, as an fp32 value (packed BF16
+// abs-max, then the larger magnitude of the two lanes).
 __device__ __forceinline__ float group_amax(const uint32_t (&w)[8]) {
-  uint32_t m = max_u16x2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu);
+  uint32_t m = absmax_bf16x2(w[0], w[1]);
 #pragma unroll
-  for (int i = 2; i < 8; ++i) m = max_u16x2(m, w[i] & 0x7FFF7FFFu);
-  const uint32_t lo = m & 0xFFFFu, hi = m >> 16;
+  for (int i = 2; i < 8; ++i) m = absmax_bf16x2(m, w[i]);
+  const uint32_t lo = m & 0x7FFFu, hi = (m >> 16) & 0x7FFFu;
   return __uint_as_float((lo > hi ? lo : hi) << 16);
 }
 
