@@ -546,6 +546,40 @@ def cpu_baseline(sample_seconds: float = 10.0):
                       f"{el:.1f} s, single-threaded C oracle, fp64 statistics)"}
 
 
+def _oracle_rows_for(seconds: float, seed: int):
+    """Worker of cpu_baseline_all_cores: the single-threaded oracle on 256-row chunks for
+    about `seconds`; returns (rows, elapsed)."""
+    import oracle
+    import workloads as W
+    c = W.CONFIGS["nss_qwen"]
+    inp = W.config_inputs("nss_qwen", rows=256, seed=seed)
+    rows_done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.nss_fp8(inp["x"], inp["scale"], inp["shift"], c["input_scale"])
+        rows_done += inp["x"].shape[0]
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return rows_done, el
+
+
+def cpu_baseline_all_cores(sample_seconds: float = 10.0):
+    """The same oracle, one process per host core (spawned), each on its own row chunks."""
+    import multiprocessing as mp
+    n = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(n) as pool:
+        res = pool.starmap(_oracle_rows_for, [(sample_seconds, 100 + i) for i in range(n)])
+    wall = time.perf_counter() - t0
+    rows = sum(r for r, _ in res)
+    el = max(e for _, e in res)
+    return {"value": rows / el, "unit": "rows/s", "cores": n, "kind": "oracle",
+            "host": host_cpu(),
+            "sample": f"{rows} rows of the nss_fp8 Qwen-Image workload, {n} spawned processes "
+                      f"x ~{sample_seconds:.0f} s of 256-row chunks (rate over the slowest "
+                      f"process's time; {wall:.1f} s wall with start-up)"}
+
+
 def roofline_entry(case: Case, ms_per_launch: float, peak: float, peak_src: str):
     achieved = case.alg_bytes / (ms_per_launch / 1e3) / 1e9
     traffic = ncu_traffic(case.ncu_key)
@@ -642,6 +676,7 @@ def run_ours(args):
         line["kernels"] = ks
     if rank == 0 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(args.cpu_seconds)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
