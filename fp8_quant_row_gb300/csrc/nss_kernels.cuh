@@ -260,7 +260,8 @@ template <int V, int P, bool kSmallTest>
 __device__ __forceinline__ void row_outputs(const uint4* stage, const float4* tab,
                                             const RowConst& kc, f2 mu2, f2 r2, f2 c2, f2 inv2,
                                             uint4* yr, uint2* qr) {
-#pragma unroll 2
+  // unrolled 6 deep (measured: 2 -> 6 gains 3-4 %; the full 12 overflows the i-cache)
+#pragma unroll 6
   for (int j = 0; j < V; ++j) {
     const uint4 xv = stage[j * 32];
     const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -450,7 +451,8 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
     const RowOffsets off = row_offsets(mexp);
     f2 sx = f2_make(off.K, off.K), sq = f2_make(off.K2, off.K2), ex = f2_make(0.0f, 0.0f),
        eq = ex;
-#pragma unroll 2
+    // 4 deep for one warp per row, 6 with two (measured best for each)
+#pragma unroll(WPR == 1 ? 4 : 6)
     for (int j = 0; j < V; ++j) {
       const uint4 xv = stage[j * 32];
       const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
