@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
     if constexpr (RESID) {
       // residual_out replaces x in the stage; each lane rewrites only its own chunks.
       uint4* ro = reinterpret_cast<uint4*>(p.residual_out + row_off) + lane;
-#pragma unroll 2
+#pragma unroll 6
       for (int j = 0; j < V; ++j) {
         const uint4 xv = stage[j * 32], rv = stage[(PC / 8) + j * 32];
         const float4 gf = lds128(tab + (j * P + 4) * 32);
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
     // are accumulated separately. v*v is exact (8-bit significands). max|x| comes from a
     // packed bf16 abs-max (max.xorsign.abs.bf16x2) over the row part, reduced over the warp.
     uint32_t m2 = 0;
-#pragma unroll 4
+#pragma unroll
     for (int j = 0; j < V; ++j) {
       const uint4 xv = stage[j * 32];
       m2 = absmax_bf16x2(m2, absmax_bf16x2(absmax_bf16x2(xv.x, xv.y), absmax_bf16x2(xv.z, xv.w)));
