@@ -229,10 +229,20 @@ __device__ __forceinline__ dd warp_sum_offset(f2 s, f2 e, float K, int ek, bool 
   const int ue = __float2int_rn(scale2(el, 43 - ek));
   const int U = int(__reduce_add_sync(0xffffffffu, uint32_t(u)));
   const int UE = int(__reduce_add_sync(0xffffffffu, uint32_t(ue)));
-  // total = U * 2^(ek - shift) + UE * 2^(ek - 43) = T * 2^(ek - 43), T exact in int64
-  const long long T = (static_cast<long long>(U) << (43 - shift)) + UE;
-  const float hi = __ll2float_rn(T);
-  const float lo = __ll2float_rn(T - __float2ll_rz(hi));  // exact: |T - hi| < 2^24
+  // total = U * 2^(ek - shift) + UE * 2^(ek - 43) = T * 2^(ek - 43) with the integer
+  // T = V * 2^k + W, k = 43 - shift, V = U + floor(UE / 2^k), W = UE mod 2^k (|U| < 2^29,
+  // |UE| < 2^31 by the bounds on K). T is formed in 32-bit pieces that are exact in fp32
+  // (64-bit integer <-> float conversions run on the slow fp64 pipe): a = (V with its low 8
+  // bits cleared) * 2^k, and the two parts of m = (V mod 2^8) * 2^k + W < 2^28.
+  const int k = 43 - shift;
+  const int V = U + (UE >> k);
+  const int m = ((V & 0xFF) << k) | (UE & ((1 << k) - 1));
+  const float a = __fmul_rn(__int2float_rn(V & ~0xFF), pow2f(k));
+  float sa, ea;
+  two_sum(a, __int2float_rn(m & ~0xF), sa, ea);
+  // hi + lo == T exactly while |a + (m & ~0xF)| < 2^28 (then ea == 0), else within 2^-47 |T|
+  float hi, lo;
+  fast_two_sum(sa, __fadd_rn(ea, __int2float_rn(m & 0xF)), hi, lo);
   dd r;
   two_sum(scale2(hi, ek - 43), scale2(lo, ek - 43), r.hi, r.lo);
   return r;
