@@ -103,14 +103,14 @@ __device__ __forceinline__ dd dd_add(dd a, dd b) {
 
 __device__ __forceinline__ dd dd_neg(dd a) { return dd{-a.hi, -a.lo}; }
 
-// a / c for a small exact float c (the row width): q1 = RN(a.hi / c), exact remainder,
-// second quotient digit.
-__device__ __forceinline__ dd dd_div_f(dd a, float c) {
-  const float q1 = __fdiv_rn(a.hi, c);
-  float p, pe;
-  two_prod(q1, c, p, pe);
-  const float rem = __fadd_rn(__fsub_rn(__fsub_rn(a.hi, p), pe), a.lo);
-  const float q2 = __fdiv_rn(rem, c);
+// a / c for a positive integer c < 2^16 (the row width) given rc = RN(1/c): q1 = RN(a.hi * rc)
+// lies within two ulps of a.hi / c, so the remainder a.hi - q1 c (at most 2 ulp(q1) c, on the
+// grid of ulp(q1) times the lowest set bit of c) is exact in one FMA while q1 is normal; the
+// second quotient digit comes from it. No division instruction sits on the row's critical path.
+__device__ __forceinline__ dd dd_div_f(dd a, float c, float rc) {
+  const float q1 = __fmul_rn(a.hi, rc);
+  const float rem = __fadd_rn(__fmaf_rn(-q1, c, a.hi), a.lo);
+  const float q2 = __fmul_rn(rem, rc);
   dd r;
   fast_two_sum(q1, q2, r.hi, r.lo);
   return r;
@@ -152,9 +152,11 @@ struct RowConst {
   float t_small;   // |t| below this goes to the exact path (absolute error dominates there)
 };
 
-__device__ __forceinline__ RowConst row_constants(dd sum, dd sumsq, float cols, float eps) {
-  const dd mu = dd_div_f(sum, cols);
-  const dd e2 = dd_div_f(sumsq, cols);
+// rcols = RN(1 / cols).
+__device__ __forceinline__ RowConst row_constants(dd sum, dd sumsq, float cols, float rcols,
+                                                  float eps) {
+  const dd mu = dd_div_f(sum, cols, rcols);
+  const dd e2 = dd_div_f(sumsq, cols, rcols);
   dd var = dd_add(e2, dd_neg(dd_sqr(mu)));
   if (!(var.hi > 0.0f)) var = dd{0.0f, 0.0f};  // exact zero for constant rows; no negatives
   float ws, we;

@@ -401,6 +401,7 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
   const float inv = __frcp_rn(__ldg(p.input_scale));
   const f2 inv2 = f2_make(inv, inv);
   const float colsf = float(C);
+  const float rcols = __frcp_rn(colsf);
   const float4* tab = table + size_t(part) * V * P * 32 + lane;
   int parity = 0;
 
@@ -498,7 +499,7 @@ __global__ void __launch_bounds__(kTunedMaxThreads, 1)
       }
       parity ^= 1;
     }
-    const RowConst kc = row_constants(s1, s2, colsf, p.eps);
+    const RowConst kc = row_constants(s1, s2, colsf, rcols, p.eps);
     const f2 mu2 = f2_make(kc.mu_hi, kc.mu_hi), r2 = f2_make(kc.r_hi, kc.r_hi),
              c2 = f2_make(kc.c, kc.c);
 
@@ -526,6 +527,7 @@ __global__ void __launch_bounds__(kNssThreads) nss_generic_kernel(const NssParam
   wait_for_producers();
   const float inv = __frcp_rn(__ldg(p.input_scale));
   const float colsf = float(p.cols);
+  const float rcols = __frcp_rn(colsf);
 
   for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
     const int64_t m = p.mod_rows > 0 ? r / p.mod_rows : 0;
@@ -564,7 +566,7 @@ __global__ void __launch_bounds__(kNssThreads) nss_generic_kernel(const NssParam
         s2 = dd_add(s2, dd{aw.z, aw.w});
       }
     }
-    const RowConst k = row_constants(s1, s2, colsf, p.eps);
+    const RowConst k = row_constants(s1, s2, colsf, rcols, p.eps);
     for (int c = threadIdx.x; c < chunks; c += kNssThreads) {
       const uint4 n = normalise8(srow[c], k);
       const uint4 sc = *(reinterpret_cast<const uint4*>(p.scale + mod_off) + c);
