@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -53,12 +54,22 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and blank-line or indentation differences (string
+    literals are kept as they are; the sources' asm strings hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code (comments excluded), which keys the committed ncu
+    counters: a change to the code makes them stale, a change to a comment does not."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_quant_row_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

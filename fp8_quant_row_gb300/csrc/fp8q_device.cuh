@@ -4,7 +4,7 @@
 //   cvt.rn.bf16x2.f32           two fp32 -> two bf16, round-to-nearest-even
 //   cvt.rn.satfinite.e4m3x2.f32 two fp32 -> two E4M3 codes, RNE, saturating to +-448
 //   fma.rn.bf16x2               two single-rounded bf16 fused multiply-adds
-// Double-float ("dd") helpers carry the LayerNorm statistics at ~2^-45 relative precision
+// Double-float ("dd") helpers form the LayerNorm row constants at ~2^-45 relative precision
 // with fp32 arithmetic only (GB300's fp64 rate is far too low for a per-element path). They
 // follow the error-free transformations of Knuth (TwoSum), Dekker (FastTwoSum) and the
 // FMA-based TwoProduct; all operations use explicit _rn intrinsics so the compiler can

@@ -12,9 +12,10 @@
 // holds V 16-byte chunks of it in registers (chunk j of lane l covers columns
 // [(j*32 + l)*8, +8) of the warp's part), so every global load and store of a warp is one
 // contiguous 512-byte (bf16) or 256-byte (e4m3) segment. The row sums sum(x) and sum(x^2)
-// are accumulated error-free (TwoSum, on packed fp32 pairs) per lane and reduced across the
-// warp by an xor butterfly of double-float additions (commutative, so every lane ends with
-// bit-identical row constants). Each warp streams its rows through a two-stage cp.async ring
+// are accumulated per lane with FastTwoSum on packed fp32 pairs started at power-of-two
+// offsets (every rounding error exact, the errors summed apart in fp32), and the lanes'
+// totals are added as integers (redux.sync), so every lane ends with bit-identical row
+// constants. Each warp streams its rows through a two-stage cp.async ring
 // in shared memory, so the next row is in flight while the current one is processed.
 // RN(1 + scale) and shift are expanded once per CTA into shared memory as fp32 in lane-major
 // order (each warp-wide 16-byte shared load is conflict-free). CTAs are persistent, own a

@@ -91,8 +91,10 @@ typedef enum fp8q_status {
  *   cols        multiple of 8, 8 <= cols <= 32768 (3072 and 6144 take the tuned path)
  *   eps         >= 0 and finite (1e-6 on the pages)
  *   Aliasing: no output may overlap any input or the other output (FP8Q_ERR_ALIAS).
- *   Statistics are exact to about 2^-45 relative; each normalised value is rounded to BF16
- *   as the exact value would be, except when that value lies within ~2^-44 relative of a
+ *   The row sums are formed error-free except for an fp32 sum of per-element rounding
+ *   errors: the mean comes out exact on the workload rows and the variance within about
+ *   2^-43 * (max|x| / sigma)^2 relative. Each normalised value is rounded to BF16 as the exact
+ *   value would be, except when that value lies within about that relative distance of a
  *   BF16 rounding midpoint.
  */
 fp8q_status fp8q_nss_fp8(void* y_bf16, uint8_t* q_e4m3, const void* x_bf16,
