@@ -327,6 +327,11 @@ __device__ __forceinline__ uint32_t rope_word(uint32_t nw, float c, float s) {
 // ahead, with no CTA-wide barrier after the start: item = (token, type), type one of the
 // eight-head blocks of Q, of K or of V. A Q/K item brings 2 KB of values (planar) and the
 // token's cos/sin row into the warp's slot; a V item brings 2 KB that go straight back out.
+// Type of the item with remainder r < 3 * octs (r / octs, by comparison: no division).
+__device__ __forceinline__ int item_type(int r, int octs) {
+  return int(r >= octs) + int(r >= 2 * octs);
+}
+
 constexpr int kQkvDepth = 4;           // slots per warp
 constexpr int kQkvWeightBytes = 2048;  // four fp32 RMSNorm weight vectors
 constexpr int kQkvSlotBytes = 2560;    // 8 heads x 256 B + cos/sin 512 B
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams 
     const bool is_txt = it.token < P.txt.tokens;
     auto sel = [is_txt](auto a, auto b) { return is_txt ? a : b; };
     const int64_t row = is_txt ? it.token : it.token - P.txt.tokens;
-    const int type = it.r / octs, oc = it.r - (it.r / octs) * octs;
+    const int type = item_type(it.r, octs), oc = it.r - type * octs;
     const uint16_t* base = type == 0 ? sel(P.txt.q, P.img.q)
                          : type == 1 ? sel(P.txt.k, P.img.k) : sel(P.txt.v, P.img.v);
     const uint16_t* src = base + row * sel(P.txt.ld, P.img.ld) + oc * 8 * kHeadDim;
@@ -419,7 +424,7 @@ __global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams 
     __syncwarp();
     const uint8_t* sl = ring + int(k % kQkvDepth) * kQkvSlotBytes;
     const Item it = cur;
-    const int type = it.r / octs, oc = it.r - type * octs;
+    const int type = item_type(it.r, octs), oc = it.r - type * octs;
     const bool is_txt = it.token < P.txt.tokens;
     if (type == 2) {
       uint16_t* dst = P.jv + it.token * row_len + oc * 8 * kHeadDim;
