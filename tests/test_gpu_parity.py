@@ -410,7 +410,8 @@ def test_qkv_epilogue_configs(name):
 
 @pytest.mark.parametrize("tt,it,heads,extra", [(0, 64, 24, 0), (37, 0, 24, 0), (3, 5, 1, 16),
                                                (2, 9, 5, 48), (7, 4, 7, 0), (1, 1, 13, 16),
-                                               (16, 16, 96, 0)])
+                                               (16, 16, 96, 0), (5, 11, 64, 16), (4, 7, 57, 0),
+                                               (3, 6, 65, 0)])
 def test_qkv_epilogue_shapes(tt, it, heads, extra):
     d = W.qkv_inputs(tt, it, heads, seed=tt * 31 + it + heads, extra_cols=extra)
     d["img"]["eps"] = 1e-5
