@@ -153,8 +153,13 @@ fp8q_status launch_tuned(const fp8q::NssParams& p, const DeviceInfo& dev, int64_
   using L = fp8q::TunedLayout<V, WPR, RESID>;
   auto* fn = fp8q::nss_tuned_kernel<V, WPR, RESID, HAS_BIAS>;
   *launched = false;
-  // As many warps per CTA (one CTA per SM) as the shared-memory ring allows, up to 16.
-  int nw = fp8q::kTunedMaxThreads / 32;
+  // As many warps per CTA (one CTA per SM) as the shared-memory ring allows, up to 24 where
+  // the kernel is built for it; below 16 rows per SM at most 16 (width 3072, two warps per
+  // row, 16 -> 24 warps: 2048 rows 10.41 -> 10.70 us, 3072 rows 13.25 -> 13.06 us, 4608 rows
+  // 16.85 -> 16.59 us).
+  int nw = fp8q::tuned_threads<V, WPR, RESID>() / 32;
+  if (p.rows < 16 * int64_t(dev.sms) && nw > fp8q::kTunedMaxThreads / 32)
+    nw = fp8q::kTunedMaxThreads / 32;
   while (nw >= WPR && L::smem_bytes(nw) > size_t(dev.smem_optin)) nw -= WPR;
   nw -= nw % WPR;
   if (nw < WPR) return FP8Q_OK;
@@ -196,13 +201,16 @@ fp8q_status dispatch_ln(const fp8q::NssParams& p, const DeviceInfo& dev, int64_t
                         cudaStream_t stream) {
   bool launched = false;
   fp8q_status st = FP8Q_OK;
-  // One warp per row at 3072 (the row is 96 elements per lane); two warps per row for the
-  // residual variant, whose ring stages hold two rows' worth of input (x and residual): half
-  // rows per warp let twice as many warps fit in shared memory.
   // Up to four rows per SM the CTA-per-row kernel (eight warps share a row) has the lower
   // latency: 4.2 vs 9.8 us at 127 rows, 6.3 vs 7.2 at 512, 8.3 vs 8.2 at 768 (width 3072).
+  // At width 3072 two warps share a row up to 48 rows per SM: each warp's chain of per-row
+  // work is half as long, which pays while a warp has few rows (width 3072, one vs two warps
+  // per row: 1024 rows 9.02 -> 7.44 us, 4608 rows 16.97 -> 16.74 us, 6144 rows 21.16 ->
+  // 20.54 us, but 9216 rows 27.47 -> 28.14 us). The residual variant always uses two: its
+  // ring stages hold two rows' worth of input (x and residual), and half rows per warp let
+  // twice as many warps fit in shared memory.
   if (p.rows <= 4 * int64_t(dev.sms)) return launch_generic<RESID, HAS_BIAS>(p, dev, stream);
-  if (p.cols == 3072 && RESID)
+  if (p.cols == 3072 && (RESID || p.rows <= 48 * int64_t(dev.sms)))
     st = launch_tuned<6, 2, RESID, HAS_BIAS>(p, dev, n_mod, stream, &launched);
   else if (p.cols == 3072)
     st = launch_tuned<12, 1, RESID, HAS_BIAS>(p, dev, n_mod, stream, &launched);

@@ -136,6 +136,13 @@ __device__ __forceinline__ void modulate_quant8(const uint4& n, const float* ops
 // ------------------------------------------------------------------------------------------
 
 constexpr int kTunedMaxThreads = 512;
+// The plain LayerNorm with two warps per row at width 3072 (3 KB stages) fits 24 warps in
+// shared memory and within 85 registers; the other instantiations stay at 16 warps (the
+// residual kernels need more registers, the wider stages more shared memory).
+template <int V, int WPR, bool RESID>
+__host__ __device__ constexpr int tuned_threads() {
+  return (!RESID && V == 6 && WPR == 2) ? 768 : kTunedMaxThreads;
+}
 constexpr int kMaxTableUnitsPerThread = 4;  // the host guarantees 4 * threads >= table units
 constexpr int kStages = 2;
 
@@ -309,7 +316,7 @@ __device__ __forceinline__ void row_outputs(const uint4* stage, const float4* ta
 }
 
 template <int V, int WPR, bool RESID, bool HAS_BIAS>
-__global__ void __launch_bounds__(kTunedMaxThreads, 1)
+__global__ void __launch_bounds__(tuned_threads<V, WPR, RESID>(), 1)
     nss_tuned_kernel(const NssParams p, const int64_t n_mod) {
   using L = TunedLayout<V, WPR, RESID>;
   constexpr int C = L::kCols;

@@ -110,6 +110,18 @@ def test_nss_shapes_and_ragged_rows(rows, cols, mod_rows):
     check_ln(yg, qg, yr, qr, 0.05, f"shape {rows}x{cols}/{mod_rows}")
 
 
+def test_nss_width_3072_one_warp_per_row():
+    """Above 48 rows per SM the width-3072 LayerNorm gives each warp a whole row (below, two
+    warps share one); a ragged row count and three modulation groups."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = 50 * sms + 37
+    mod_rows = (rows + 2) // 3
+    inp = W.nss_inputs(rows, 3072, seed=5, n_mod=3, outlier_channels=30)
+    yg, qg = run_nss(inp, 0.0625, mod_rows=mod_rows)
+    yr, qr = oracle.nss_fp8(inp["x"], inp["scale"], inp["shift"], 0.0625, mod_rows=mod_rows)
+    check_ln(yg, qg, yr, qr, 0.0625, f"one warp per row, {rows} rows")
+
+
 def test_nss_degenerate_rows():
     """Constant rows (var = 0), tiny spreads (var ~ eps), large means, huge values that
     saturate the E4M3 encode, zero rows."""
