@@ -549,3 +549,84 @@ def test_calls_capture_into_a_cuda_graph_and_replay():
     for i, (u, v) in enumerate(zip(got, want)):
         assert np.array_equal(u, v), i
     assert not np.array_equal(got[0], G.host_u16(G.dev_bf16(rng_inputs[0]["x"])))  # really replayed
+
+
+# ------------------------------------------------------------------------------------------
+# seeded random sweeps: shapes, row counts across the kernel choices, scales, eps, value
+# ranges and modulation groups drawn from a fixed seed (the same cases on every run)
+# ------------------------------------------------------------------------------------------
+
+def _random_scale(rng):
+    return float(np.float32(10 ** rng.uniform(-2.5, 0.5)))
+
+
+def test_random_sweep_nss():
+    rng = np.random.default_rng(2026)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for case in range(24):
+        cols = int(rng.choice([3072, 6144, 8 * int(rng.integers(1, 600))]))
+        tuned = cols in (3072, 6144)
+        rows = int(rng.integers(1, 6 * sms if tuned else 300))  # across the 4-rows-per-SM split
+        mod_rows = 0 if rng.random() < 0.5 else max(1, rows // int(rng.integers(1, 4)))
+        n_mod = (rows + mod_rows - 1) // mod_rows if mod_rows else 1
+        s, eps = _random_scale(rng), float(rng.choice([1e-6, 1e-5, 0.0]))
+        inp = W.nss_inputs(rows, cols, seed=1000 + case, n_mod=n_mod,
+                           outlier_channels=int(rng.integers(0, cols // 50 + 1)),
+                           x_std=float(10 ** rng.uniform(-3, 2)))
+        yg, qg = run_nss(inp, s, mod_rows=mod_rows, eps=eps)
+        yr, qr = oracle.nss_fp8(inp["x"], inp["scale"], inp["shift"], s, mod_rows=mod_rows,
+                                eps=eps)
+        check_ln(yg, qg, yr, qr, s, f"random {case}: {rows}x{cols}/{mod_rows} s={s} eps={eps}")
+
+
+def test_random_sweep_scale_residual_and_bias_mul_add():
+    rng = np.random.default_rng(2027)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for case in range(12):
+        cols = int(rng.choice([3072, 6144, 8 * int(rng.integers(1, 400))]))
+        rows = int(rng.integers(1, 6 * sms if cols in (3072, 6144) else 200))
+        mod_rows = 0 if rng.random() < 0.5 else max(1, rows // int(rng.integers(1, 4)))
+        n_mod = (rows + mod_rows - 1) // mod_rows if mod_rows else 1
+        with_bias, in_place, s = bool(rng.random() < 0.7), bool(rng.random() < 0.3), _random_scale(rng)
+        inp = W.residual_inputs(rows, cols, seed=2000 + case, n_mod=n_mod)
+        rg, yg, qg = run_scale_residual(inp, s, with_bias=with_bias, in_place=in_place,
+                                        mod_rows=mod_rows)
+        rr, yr, qr = oracle.scale_residual_nss_fp8(inp["x"], inp["residual"],
+                                                   inp["bias"] if with_bias else None,
+                                                   inp["gate"], inp["scale"], inp["shift"], s,
+                                                   mod_rows=mod_rows)
+        what = f"random {case}: {rows}x{cols}/{mod_rows} bias={with_bias} in_place={in_place}"
+        assert np.array_equal(rg, rr), what
+        check_ln(yg, qg, yr, qr, s, what)
+        y = G.Guarded((rows, cols), torch.bfloat16)
+        fq().bias_mul_add(G.dev_bf16(inp["x"]), G.dev_bf16(inp["bias"]),
+                          G.dev_bf16(inp["gate"][0]), G.dev_bf16(inp["residual"]), y=y.tensor)
+        torch.cuda.synchronize()
+        assert y.intact()
+        assert np.array_equal(G.host_u16(y.tensor), oracle.bias_mul_add(
+            inp["x"], inp["bias"], inp["gate"][0], inp["residual"])), what
+
+
+def test_random_sweep_token_cat_fp8_and_nvfp4():
+    rng = np.random.default_rng(2028)
+    for case in range(16):
+        rows = int(rng.integers(1, 400))
+        a_cols, m_cols = 64 * int(rng.integers(1, 100)), 64 * int(rng.integers(1, 300))
+        inp = W.token_cat_inputs(rows, a_cols, m_cols, seed=3000 + case)
+        s = _random_scale(rng)
+        assert np.array_equal(run_token_cat(inp["a"], inp["m"], s),
+                              oracle.token_cat_fp8(inp["a"], inp["m"], s)), f"fp8 random {case}"
+        g = float(np.float32(10 ** rng.uniform(-3, 6)))
+        check_nvfp4(inp["a"], inp["m"], g, f"nvfp4 random {case}: {rows}x{a_cols}+{m_cols} g={g}")
+
+
+def test_random_sweep_qkv_epilogue():
+    rng = np.random.default_rng(2029)
+    for case in range(12):
+        heads = int(rng.integers(1, 71))   # both the ring (<= 64 heads) and the per-token kernel
+        tt, it = int(rng.integers(0, 40)), int(rng.integers(0, 80))
+        if tt + it == 0:
+            it = 1
+        d = W.qkv_inputs(tt, it, heads, seed=4000 + case, extra_cols=16 * int(rng.integers(0, 4)))
+        d["txt"]["eps"] = float(rng.choice([1e-6, 1e-5]))
+        check_qkv(d, heads, f"random {case}: {tt}+{it}x{heads}")
