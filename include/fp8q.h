@@ -19,7 +19,7 @@
  *     only enqueues work on `stream` (0 = the legacy default stream). Outputs are complete
  *     when that stream reaches the launch.
  *   - Every tensor pointer must be 16-byte aligned (FP8Q_ERR_ALIGN otherwise); the NVFP4
- *     entry point needs 32 bytes for its data pointers.
+ *     and QKV entry points need 32 bytes for their data pointers (see each call).
  *   - rows == 0 returns FP8Q_OK without touching any pointer or launching anything.
  *   - Argument errors are reported synchronously, before any launch, with a status code; a
  *     failed launch returns FP8Q_ERR_CUDA (fp8q_last_cuda_error() gives the cudaError_t).
