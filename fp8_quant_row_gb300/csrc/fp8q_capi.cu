@@ -172,7 +172,7 @@ fp8q_status launch_tuned(const fp8q::NssParams& p, const DeviceInfo& dev, int64_
   const int rows_per_iter = nw / WPR;
   int64_t need = (p.rows + rows_per_iter - 1) / rows_per_iter;
   // Fewer rows than a full wave: spread them over all SMs rather than filling a few CTAs, so
-  // each SM's row finishes sooner (one warp computes a whole row).
+  // each SM's rows finish sooner (a warp or a warp pair computes a whole row).
   if (need < dev.sms) need = p.rows < dev.sms ? p.rows : dev.sms;
   const int64_t cap = int64_t(dev.sms) * bps;
   int64_t grid = need > n_mod ? need : n_mod;
@@ -202,7 +202,8 @@ fp8q_status dispatch_ln(const fp8q::NssParams& p, const DeviceInfo& dev, int64_t
   bool launched = false;
   fp8q_status st = FP8Q_OK;
   // Up to four rows per SM the CTA-per-row kernel (eight warps share a row) has the lower
-  // latency: 4.2 vs 9.8 us at 127 rows, 6.3 vs 7.2 at 512, 8.3 vs 8.2 at 768 (width 3072).
+  // latency (width 3072, against the tuned kernel with one warp per row: 4.2 vs 9.8 us at 127
+  // rows, 6.3 vs 7.2 at 512, 8.3 vs 8.2 at 768).
   // At width 3072 two warps share a row up to 48 rows per SM: each warp's chain of per-row
   // work is half as long, which pays while a warp has few rows (width 3072, one vs two warps
   // per row: 1024 rows 9.02 -> 7.44 us, 4608 rows 16.97 -> 16.74 us, 6144 rows 21.16 ->
