@@ -122,6 +122,18 @@ def test_nss_width_3072_one_warp_per_row():
     check_ln(yg, qg, yr, qr, 0.0625, f"one warp per row, {rows} rows")
 
 
+def test_nss_kernel_choices_give_identical_bits():
+    """The row count picks the kernel (CTA per row up to 4 rows per SM; two warps per row with
+    16 or, from 16 rows per SM, 24 warps; one warp per row above 48 rows per SM). Across each
+    boundary the same leading rows must come out bit for bit the same."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for n in (4 * sms, 16 * sms - 1, 48 * sms):
+        inp = W.nss_inputs(n + 1, 3072, seed=n, outlier_channels=30)
+        a = run_nss({k: v[:n] if k == "x" else v for k, v in inp.items()}, 0.0625)
+        b = run_nss(inp, 0.0625)
+        assert np.array_equal(a[0], b[0][:n]) and np.array_equal(a[1], b[1][:n]), f"{n} vs {n + 1}"
+
+
 def test_nss_degenerate_rows():
     """Constant rows (var = 0), tiny spreads (var ~ eps), large means, huge values that
     saturate the E4M3 encode, zero rows."""
