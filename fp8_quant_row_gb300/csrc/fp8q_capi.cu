@@ -201,16 +201,16 @@ fp8q_status dispatch_ln(const fp8q::NssParams& p, const DeviceInfo& dev, int64_t
                         cudaStream_t stream) {
   bool launched = false;
   fp8q_status st = FP8Q_OK;
-  // Up to four rows per SM the CTA-per-row kernel (eight warps share a row) has the lower
-  // latency (width 3072, against the tuned kernel with one warp per row: 4.2 vs 9.8 us at 127
-  // rows, 6.3 vs 7.2 at 512, 8.3 vs 8.2 at 768).
+  // Up to two rows per SM the CTA-per-row kernel (eight warps share a row) has the lower
+  // latency (width 3072, against the tuned kernel with two warps per row: 4.19 vs 4.58 us at
+  // 153 rows, 4.53 vs 4.83 at 256; above, 4.91 vs 5.25 at 400, 5.26 vs 6.12 at 512).
   // At width 3072 two warps share a row up to 48 rows per SM: each warp's chain of per-row
   // work is half as long, which pays while a warp has few rows (width 3072, one vs two warps
   // per row: 1024 rows 9.02 -> 7.44 us, 4608 rows 16.97 -> 16.74 us, 6144 rows 21.16 ->
   // 20.54 us, but 9216 rows 27.47 -> 28.14 us). The residual variant always uses two: its
   // ring stages hold two rows' worth of input (x and residual), and half rows per warp let
   // twice as many warps fit in shared memory.
-  if (p.rows <= 4 * int64_t(dev.sms)) return launch_generic<RESID, HAS_BIAS>(p, dev, stream);
+  if (p.rows <= 2 * int64_t(dev.sms)) return launch_generic<RESID, HAS_BIAS>(p, dev, stream);
   if (p.cols == 3072 && (RESID || p.rows <= 48 * int64_t(dev.sms)))
     st = launch_tuned<6, 2, RESID, HAS_BIAS>(p, dev, n_mod, stream, &launched);
   else if (p.cols == 3072)

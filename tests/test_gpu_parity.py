@@ -123,11 +123,11 @@ def test_nss_width_3072_one_warp_per_row():
 
 
 def test_nss_kernel_choices_give_identical_bits():
-    """The row count picks the kernel (CTA per row up to 4 rows per SM; two warps per row with
+    """The row count picks the kernel (CTA per row up to 2 rows per SM; two warps per row with
     16 or, from 16 rows per SM, 24 warps; one warp per row above 48 rows per SM). Across each
     boundary the same leading rows must come out bit for bit the same."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for n in (4 * sms, 16 * sms - 1, 48 * sms):
+    for n in (2 * sms, 16 * sms - 1, 48 * sms):
         inp = W.nss_inputs(n + 1, 3072, seed=n, outlier_channels=30)
         a = run_nss({k: v[:n] if k == "x" else v for k, v in inp.items()}, 0.0625)
         b = run_nss(inp, 0.0625)
@@ -578,7 +578,7 @@ def test_random_sweep_nss():
     for case in range(24):
         cols = int(rng.choice([3072, 6144, 8 * int(rng.integers(1, 600))]))
         tuned = cols in (3072, 6144)
-        rows = int(rng.integers(1, 6 * sms if tuned else 300))  # across the 4-rows-per-SM split
+        rows = int(rng.integers(1, 6 * sms if tuned else 300))  # across the 2-rows-per-SM split
         mod_rows = 0 if rng.random() < 0.5 else max(1, rows // int(rng.integers(1, 4)))
         n_mod = (rows + mod_rows - 1) // mod_rows if mod_rows else 1
         s, eps = _random_scale(rng), float(rng.choice([1e-6, 1e-5, 0.0]))
