@@ -11,10 +11,20 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfp8q.so")
 SOURCES = [os.path.join(CSRC, "fp8q_capi.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fp8q_device.cuh", "nss_kernels.cuh",
-                                                  "elementwise_kernels.cuh",
-                                                  "nvfp4_kernels.cuh")] + \
-    [os.path.join(INCLUDE, "fp8q.h")]
+
+
+def deps() -> list:
+    """Every file the build reads: all of csrc/ (sources and the headers they include) and
+    the public headers. Taken from the directories at call time, so a new or renamed kernel
+    header can never be left out of the staleness check."""
+    out = []
+    for d in (CSRC, INCLUDE):
+        for f in sorted(os.listdir(d)):
+            if f.endswith((".cu", ".cuh", ".h", ".hpp")):
+                out.append(os.path.join(d, f))
+    return out
+
+
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 # The CUDA runtime is linked shared (soname libcudart.so.13): inside a process that already
@@ -37,7 +47,7 @@ def up_to_date() -> bool:
     if not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(d) <= t for d in DEPS)
+    return all(os.path.getmtime(d) <= t for d in deps())
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
