@@ -11,6 +11,7 @@ library's sm_103a kernels; there is no CPU or eager fallback.
     q = token_cat_fp8(attention, mlp, input_scale)
     q4, sf = token_cat_nvfp4(attention, mlp, global_scale)            # uint8 codes / scales
     jq, jk, jv = qkv_epilogue(txt, img, heads)      # per-head QK RMSNorm + RoPE, joint pack
+    bits = device_error()                           # 0 unless a bounded kernel wait ran out
 """
 from __future__ import annotations
 
@@ -21,7 +22,7 @@ from ._build import build
 from ._capi import Fp8qError
 
 __all__ = ["nss_fp8", "scale_residual_nss_fp8", "bias_mul_add", "token_cat_fp8",
-           "token_cat_nvfp4", "nvfp4_scale_bytes", "qkv_epilogue", "build",
+           "token_cat_nvfp4", "nvfp4_scale_bytes", "qkv_epilogue", "device_error", "build",
            "Fp8qError", "library_path"]
 
 EPS = 1e-6
@@ -202,3 +203,12 @@ def qkv_epilogue(txt: dict, img: dict, heads: int, *, out=None, stream=None):
                                        ts, ims, heads, _stream_handle(stream))
     _capi.check(st, "fp8q_qkv_epilogue")
     return out
+
+
+def device_error() -> int:
+    """Reads and clears the current device's error word (fp8q_device_error): 0 unless a
+    bounded wait inside a kernel ran out since the last call. Synchronises with the device."""
+    import ctypes
+    bits = ctypes.c_uint(0)
+    _capi.check(_capi.lib().fp8q_device_error(ctypes.byref(bits)), "fp8q_device_error")
+    return int(bits.value)

@@ -20,7 +20,7 @@ STATUS = {0: "FP8Q_OK", 1: "FP8Q_ERR_NULL", 2: "FP8Q_ERR_ALIGN", 3: "FP8Q_ERR_SH
 #: every function include/fp8q.h declares
 SYMBOLS = ("fp8q_nss_fp8", "fp8q_scale_residual_nss_fp8", "fp8q_bias_mul_add",
            "fp8q_token_cat_fp8", "fp8q_token_cat_nvfp4", "fp8q_nvfp4_scale_bytes",
-           "fp8q_qkv_epilogue",
+           "fp8q_qkv_epilogue", "fp8q_device_error",
            "fp8q_status_string", "fp8q_last_cuda_error",
            "fp8q_last_error_detail", "fp8q_version")
 
@@ -67,6 +67,8 @@ def lib():
         for name in ("fp8q_nss_fp8", "fp8q_scale_residual_nss_fp8", "fp8q_bias_mul_add",
                      "fp8q_token_cat_fp8", "fp8q_token_cat_nvfp4", "fp8q_qkv_epilogue"):
             getattr(L, name).restype = i32
+        L.fp8q_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        L.fp8q_device_error.restype = i32
         L.fp8q_status_string.argtypes = [i32]
         L.fp8q_status_string.restype = ctypes.c_char_p
         L.fp8q_last_cuda_error.argtypes = []

@@ -17,6 +17,7 @@
 #include "fp8q.h"
 #include "elementwise_kernels.cuh"
 #include "nss_kernels.cuh"
+#include "nss_ws_kernels.cuh"
 #include "nvfp4_kernels.cuh"
 #include "qkv_kernels.cuh"
 
@@ -75,22 +76,48 @@ struct OccEntry {
 };
 OccEntry g_occ[256];
 int g_occ_n = 0;
+// Dynamic shared-memory limit set on each (device, function): the limit is a property of the
+// function, not of a launch, so it only ever grows to the largest size launched (a launch
+// above the current limit is rejected; a smaller size seen later must not lower it).
+struct SmemLimit {
+  int dev;
+  const void* fn;
+  size_t limit;
+};
+SmemLimit g_lim[256];
+int g_lim_n = 0;
 std::mutex g_occ_mu;
+
+fp8q_status raise_smem_limit(int dev, const void* fn, size_t smem) {
+  SmemLimit* entry = nullptr;
+  for (int i = 0; i < g_lim_n; ++i)
+    if (g_lim[i].dev == dev && g_lim[i].fn == fn) entry = &g_lim[i];
+  if (entry && entry->limit >= smem) return FP8Q_OK;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)", (long long)smem);
+  if (entry) {
+    entry->limit = smem;
+  } else if (g_lim_n < 256) {
+    g_lim[g_lim_n++] = SmemLimit{dev, fn, smem};
+  }
+  return FP8Q_OK;
+}
 
 fp8q_status blocks_per_sm(const void* fn, int threads, size_t smem, int* blocks) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   std::lock_guard<std::mutex> lock(g_occ_mu);
+  // Checked on every call: the cached occupancy below says nothing about the current limit.
+  if (smem > 48 * 1024) {
+    const fp8q_status st = raise_smem_limit(dev, fn, smem);
+    if (st != FP8Q_OK) return st;
+  }
   for (int i = 0; i < g_occ_n; ++i)
     if (g_occ[i].dev == dev && g_occ[i].fn == fn && g_occ[i].smem == smem) {
       *blocks = g_occ[i].blocks;
       return FP8Q_OK;
     }
-  if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)", (long long)smem);
-  }
   int b = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor", (long long)smem);
@@ -183,6 +210,34 @@ fp8q_status launch_tuned(const fp8q::NssParams& p, const DeviceInfo& dev, int64_
   return launch(fn, dim3(unsigned(grid)), dim3(nw * 32), smem, stream, p, n_mod);
 }
 
+// Warp-specialised kernel: one CTA per SM (never more CTAs than rows), each owning a block
+// of rows; the ring holds as many row stages as shared memory allows, rounded down to a
+// multiple of the stage quantum (see nss_ws_kernels.cuh) and no more than the CTA's rows need.
+constexpr int kWsDepth = 1 << 30;  // rows in flight per CTA (no limit beyond the ring)
+
+template <int C, int NS, int NO>
+fp8q_status launch_ws(const fp8q::NssParams& p, const DeviceInfo& dev, int64_t n_mod,
+                      cudaStream_t stream, bool* launched) {
+  using L = fp8q::WsLayout<C, NS, NO>;
+  auto* fn = fp8q::nss_ws_kernel<C, NS, NO>;
+  *launched = false;
+  int64_t grid = std::min<int64_t>(dev.sms, p.rows);
+  if (n_mod > grid) return FP8Q_OK;  // every CTA must sit inside one modulation group
+  const int64_t rows_per_cta = (p.rows + grid - 1) / grid + 1;  // group splits add one
+  const int q = L::kStageQuantum;
+  int64_t stages = int64_t(size_t(dev.smem_optin) / L::kStageBytes) / q * q;
+  stages = std::min<int64_t>(stages, (rows_per_cta + q - 1) / q * q);
+  if (stages < q) return FP8Q_OK;
+  const size_t smem = L::smem_bytes(int(stages));
+  int bps = 0;
+  fp8q_status st = blocks_per_sm(reinterpret_cast<const void*>(fn), L::kThreads, smem, &bps);
+  if (st != FP8Q_OK) return st;
+  if (bps <= 0) return FP8Q_OK;
+  *launched = true;
+  return launch(fn, dim3(unsigned(grid)), dim3(L::kThreads), smem, stream, p, n_mod, int(stages),
+                kWsDepth);
+}
+
 template <bool RESID, bool HAS_BIAS>
 fp8q_status launch_generic(const fp8q::NssParams& p, const DeviceInfo& dev, cudaStream_t stream) {
   auto* fn = fp8q::nss_generic_kernel<RESID, HAS_BIAS>;
@@ -211,6 +266,10 @@ fp8q_status dispatch_ln(const fp8q::NssParams& p, const DeviceInfo& dev, int64_t
   // ring stages hold two rows' worth of input (x and residual), and half rows per warp let
   // twice as many warps fit in shared memory.
   if (p.rows <= 2 * int64_t(dev.sms)) return launch_generic<RESID, HAS_BIAS>(p, dev, stream);
+  if (!RESID && p.cols == 3072) {
+    st = launch_ws<3072, 7, 3>(p, dev, n_mod, stream, &launched);
+    if (st != FP8Q_OK || launched) return st;
+  }
   if (p.cols == 3072 && (RESID || p.rows <= 48 * int64_t(dev.sms)))
     st = launch_tuned<6, 2, RESID, HAS_BIAS>(p, dev, n_mod, stream, &launched);
   else if (p.cols == 3072)
@@ -518,6 +577,21 @@ fp8q_status fp8q_qkv_epilogue(void* joint_q, void* joint_k, void* joint_v,
   return launch(fp8q::qkv_epilogue_kernel, dim3(gx), dim3(fp8q::kQkvWarps * 32), 0, stream, p);
 }
 
+fp8q_status fp8q_device_error(unsigned int* bits) {
+  if (!bits) return FP8Q_ERR_NULL;
+  const DeviceInfo* dev = nullptr;
+  fp8q_status st = current_device(&dev);
+  if (st != FP8Q_OK) return st;
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, fp8q::g_device_error, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol(g_device_error)");
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(fp8q::g_device_error, &zero, sizeof zero);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol(g_device_error)");
+  *bits = v;
+  return FP8Q_OK;
+}
+
 const char* fp8q_status_string(int status) {
   switch (status) {
     case FP8Q_OK: return "ok";
@@ -536,6 +610,6 @@ int fp8q_last_cuda_error(void) { return g_last_cuda_error; }
 
 const char* fp8q_last_error_detail(void) { return g_last_detail; }
 
-int fp8q_version(void) { return 0x000200; }
+int fp8q_version(void) { return 0x000300; }
 
 }  // extern "C"

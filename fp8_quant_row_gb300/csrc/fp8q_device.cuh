@@ -348,3 +348,104 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 }  // namespace fp8q
+
+namespace fp8q {
+
+// ------------------------------------------------------------------------------------------
+// device error word, mbarriers and bulk (TMA) copies
+// ------------------------------------------------------------------------------------------
+
+// Bits set by a kernel that gave up on a wait (a wait only runs out when a phase it depends
+// on never completes, i.e. on a defect): the kernel records the bit, stops taking work and
+// returns. The host reads and clears the word with fp8q_device_error().
+constexpr unsigned kDevErrWaitTimeout = 1u;
+__device__ unsigned int g_device_error = 0u;
+
+__device__ __forceinline__ void report_device_error(unsigned bits) {
+  atomicOr(&g_device_error, bits);
+}
+
+// Upper bound of every mbarrier wait, in SM clock cycles (about two seconds at 2 GHz).
+constexpr long long kWaitLimitCycles = 1ll << 32;
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Makes initialised mbarriers visible to the other threads and to the bulk-copy unit.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// One arrival that also adds `bytes` to the transaction count the phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// True once the phase with parity `parity` has completed (the thread may be suspended for a
+// hardware-chosen time inside the instruction while it is pending).
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for a phase: false when it has not completed within kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  return true;
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to this
+// CTA's shared memory, completing as transactions on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(smem_dst)), "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Four E4M3 codes E4M3(RN(y * inv)) of two bf16 pairs, as one 32-bit word (y0 low pair in
+// bytes 0-1, y1 in bytes 2-3): two packed multiplies, two conversions, one byte permute.
+__device__ __forceinline__ uint32_t quant4(uint32_t y0, uint32_t y1, unsigned long long inv2) {
+  unsigned long long a, b;
+  asm("{\n\t.reg .b64 v;\n\tmov.b64 v, {%1, %2};\n\tmul.rn.f32x2 %0, v, %3;\n\t}"
+      : "=l"(a) : "r"(y0 << 16), "r"(y0 & 0xFFFF0000u), "l"(inv2));
+  asm("{\n\t.reg .b64 v;\n\tmov.b64 v, {%1, %2};\n\tmul.rn.f32x2 %0, v, %3;\n\t}"
+      : "=l"(b) : "r"(y1 << 16), "r"(y1 & 0xFFFF0000u), "l"(inv2));
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t.reg .f32 a0, a1, b0, b1;\n\t"
+      "mov.b64 {a0, a1}, %1;\n\tmov.b64 {b0, b1}, %2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, a1, a0;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, b1, b0;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "l"(a), "l"(b));
+  return r;
+}
+
+// RN_bf16(t) as an fp32 value: the bf16 lands in the high half, the low half is zero.
+__device__ __forceinline__ float round_bf16(float t) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(t), "f"(0.0f));
+  return __uint_as_float(r);
+}
+
+}  // namespace fp8q

@@ -226,6 +226,21 @@ fp8q_status fp8q_qkv_epilogue(void* joint_q, void* joint_k, void* joint_v,
                               const fp8q_qkv_stream* txt, const fp8q_qkv_stream* img,
                               int64_t heads, cudaStream_t stream);
 
+/* Bits of the device error word (fp8q_device_error). */
+#define FP8Q_DEVERR_WAIT_TIMEOUT 1u /* a kernel gave up on a bounded shared-memory wait */
+
+/*
+ * Reads and clears the device error word of the current device. Every wait inside the
+ * library's kernels is bounded (about two seconds of SM clock); a wait that runs out sets
+ * FP8Q_DEVERR_WAIT_TIMEOUT, and the kernel stops taking work and returns with its outputs
+ * incomplete. Only a defect can cause this: every phase a kernel waits for is completed by
+ * the same CTA (a bulk copy landing, or another warp's arrival), never by the host or another
+ * kernel. Diagnostic call, not for the hot path: it synchronises with the device
+ * (cudaMemcpyFromSymbol) and is not capturable in a CUDA graph.
+ *   bits  out  host pointer; receives the word (0: no wait ran out since the last call)
+ */
+fp8q_status fp8q_device_error(unsigned int* bits);
+
 /* Human-readable name of a status code (static string; never NULL). */
 const char* fp8q_status_string(int status);
 
@@ -236,7 +251,8 @@ int fp8q_last_cuda_error(void);
  * (thread-local static string, "" if none; overwritten by the next failure). */
 const char* fp8q_last_error_detail(void);
 
-/* Library ABI version: 0x00MMmmpp (0.2.0: token_cat_nvfp4 and qkv_epilogue added). */
+/* Library ABI version: 0x00MMmmpp (0.2.0: token_cat_nvfp4 and qkv_epilogue added; 0.3.0:
+ * fp8q_device_error added). */
 int fp8q_version(void);
 
 #ifdef __cplusplus

@@ -58,7 +58,7 @@ def test_library_is_built_for_sm_103a_only(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.fp8q_version() == 0x000200
+    assert L.fp8q_version() == 0x000300
     for s in range(8):
         assert L.fp8q_status_string(s)
     assert L.fp8q_status_string(99) == b"unknown status"
