@@ -427,8 +427,19 @@ def capture(torch, case: Case, count: int, start: int):
     return g
 
 
-def time_case(torch, case: Case, steps: int, warmup: int, use_graph=True, barrier=None):
-    """Returns (elapsed_ms, t0_wall, t1_wall) for exactly `steps` launches."""
+def windows_needed(first_window_ms: float, repeats: int, min_region_s: float) -> int:
+    """Windows to time: at least `repeats`, and enough that the timed region lasts about
+    `min_region_s` (so that the clock sampler sees it), at most 2000."""
+    per = max(first_window_ms / 1e3, 1e-6)
+    return int(min(2000, max(repeats, math.ceil(min_region_s / per))))
+
+
+def time_case(torch, case: Case, steps: int, warmup: int, use_graph=True, barrier=None,
+              repeats: int = 1, min_region_s: float = 0.0, agree=None):
+    """Times windows of exactly `steps` launches. Returns (window_ms list, t0_wall, t1_wall).
+    The first window sets how many are timed (windows_needed); `agree` (max over ranks) makes
+    every rank time the same number. Each window is bracketed by a barrier and a device
+    synchronisation and timed with CUDA events on the launch stream."""
     for i in range(warmup):
         case.launch(i)
     torch.cuda.synchronize()
@@ -446,23 +457,34 @@ def time_case(torch, case: Case, steps: int, warmup: int, use_graph=True, barrie
         torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    windows = []
+    t0 = t1 = None
+    while True:
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        if t0 is None:
+            t0 = time.time()
+        ev0.record()
+        if use_graph:
+            for g in graphs:
+                g.replay()
+        else:
+            for i in range(steps):
+                case.launch(warmup + i)
+        ev1.record()
+        torch.cuda.synchronize()
+        t1 = time.time()
+        windows.append(ev0.elapsed_time(ev1))
+        if len(windows) == 1:
+            target = windows_needed(windows[0], repeats, min_region_s)
+            if agree is not None:
+                target = agree(target)
+        if len(windows) >= target:
+            break
     if barrier:
         barrier()
-    torch.cuda.synchronize()
-    t0 = time.time()
-    ev0.record()
-    if use_graph:
-        for g in graphs:
-            g.replay()
-    else:
-        for i in range(steps):
-            case.launch(warmup + i)
-    ev1.record()
-    torch.cuda.synchronize()
-    t1 = time.time()
-    if barrier:
-        barrier()
-    return ev0.elapsed_time(ev1), t0, t1
+    return windows, t0, t1
 
 
 def e2e_measure(torch, lib, case: Case, steps: int):
@@ -645,11 +667,14 @@ def run_ours(args):
 
     sampler = ClockSampler(getattr(props, "uuid", None) and str(props.uuid))
     try:
-        ms, t0, t1 = time_case(torch, main, args.steps, args.warmup, use_graph=not args.no_graph,
-                               barrier=barrier)
+        windows, t0, t1 = time_case(torch, main, args.steps, args.warmup,
+                                    use_graph=not args.no_graph, barrier=barrier,
+                                    repeats=args.repeats, min_region_s=args.min_region_s,
+                                    agree=lambda n: int(max_over_ranks(float(n), "cuda")))
     finally:
         sampler.stop()
-    ms = max_over_ranks(ms, "cuda")
+    # headline: the median K-launch window, the slowest rank's median under torchrun
+    ms = max_over_ranks(statistics.median(windows), "cuda")
     clocks = sampler.summary(t0, t1)
     ms_step = ms / args.steps
     value = job_rows_per_s(main.rows, args.steps, world, ms)
@@ -669,25 +694,37 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline_entry(main, ms_step, peak, peak_src),
         "gpu_launches": args.steps,
+        "repeats": {"windows": len(windows), "launches_per_window": args.steps,
+                    "ms_per_step_min": round(min(windows) / args.steps, 6),
+                    "ms_per_step_median": round(statistics.median(windows) / args.steps, 6),
+                    "ms_per_step_max": round(max(windows) / args.steps, 6),
+                    "note": "value and ms_per_step are the median window (max over ranks)"},
         "clocks": clocks,
     }
     if rank == 0 and not args.skip_e2e:
         line["e2e"] = e2e_measure(torch, lib, main, max(3, min(args.steps, 200)))
+    kernels = None
     if rank == 0 and not args.skip_kernels:
-        ks = {}
+        # every other kernel of the path, the same way (200-launch windows, median of 5); the
+        # workloads are described on stderr, the line keeps a compact table at its end
+        kernels = {}
         for key, build_case in extra_cases(torch, lib, l2).items():
             case = build_case()
-            kms, _, _ = time_case(torch, case, 200, 5, use_graph=not args.no_graph)
-            per = kms / 200
-            ks[key] = {"kernel": case.name, "workload": case.describe,
-                       "us_per_launch": round(per * 1e3, 3), "rows_per_s": round(case.rows / (per / 1e3), 1),
-                       "roofline": roofline_entry(case, per, peak, peak_src)}
+            kw, _, _ = time_case(torch, case, 200, 5, use_graph=not args.no_graph, repeats=5)
+            per = statistics.median(kw) / 200
+            rl = roofline_entry(case, per, peak, peak_src)
+            kernels[key] = {"us": round(per * 1e3, 3), "frac": rl["frac"],
+                            "gbs": rl["achieved"], "traffic": rl["traffic"]}
+            log(f"kernel {key}: {case.name}: {case.describe}: {per * 1e3:.3f} us, "
+                f"{rl['achieved']} GB/s, {rl['frac']} of {peak} GB/s ({peak_src})")
             del case
             torch.cuda.empty_cache()
-        line["kernels"] = ks
     if rank == 0 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
         line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(args.cpu_seconds)
+    if kernels is not None:
+        # last key of the line, so that a reader of only the end of the output still sees it
+        line["kernels"] = {"unit": "us per launch / fraction of measured HBM", **kernels}
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -768,6 +805,10 @@ def main():
     ap.add_argument("--skip-kernels", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--repeats", type=int, default=10,
+                    help="timed windows of K launches (the headline is their median)")
+    ap.add_argument("--min-region-s", type=float, default=0.3,
+                    help="add windows until the timed region lasts this long (clock samples)")
     ap.add_argument("--profile-only", choices=("nss_qwen", "nss_tiny", "scale_residual_qwen",
                                                "token_cat_nvfp4_flux", "qkv_qwen", "qkv_flux",
                                                "bias_mul_add_qwen", "nss_flux", "token_cat_flux"),

@@ -22,7 +22,8 @@ from ._build import build
 from ._capi import Fp8qError
 
 __all__ = ["nss_fp8", "scale_residual_nss_fp8", "bias_mul_add", "token_cat_fp8",
-           "token_cat_nvfp4", "nvfp4_scale_bytes", "qkv_epilogue", "device_error", "build",
+           "token_cat_nvfp4", "nvfp4_scale_bytes", "qkv_epilogue", "device_error",
+           "row_pieces", "build",
            "Fp8qError", "library_path"]
 
 EPS = 1e-6
@@ -212,3 +213,28 @@ def device_error() -> int:
     bits = ctypes.c_uint(0)
     _capi.check(_capi.lib().fp8q_device_error(ctypes.byref(bits)), "fp8q_device_error")
     return int(bits.value)
+
+
+def row_pieces(rows: int, mod_rows: int, world: int, rank: int):
+    """The pieces of rank `rank`'s share when `rows` rows are split over `world` processes:
+    a list of (r0, r1, group). The rows are cut into `world` contiguous slices of near-equal
+    size (the first rows % world slices one row longer), and a slice is cut again wherever
+    it crosses a modulation-group boundary (a multiple of mod_rows), so every piece lies in
+    one group. Each piece is one call on x[r0:r1] with mod_rows = 0 and the scale/shift (and
+    gate) rows of `group` (0 when mod_rows is 0). Rows are independent, so the pieces of all
+    ranks together give exactly the single call's outputs; no data is exchanged."""
+    if rows < 0 or mod_rows < 0 or world < 1 or not 0 <= rank < world:
+        raise ValueError("row_pieces: need rows >= 0, mod_rows >= 0, 0 <= rank < world")
+    base, extra = divmod(rows, world)
+    r0 = rank * base + min(rank, extra)
+    r1 = r0 + base + (1 if rank < extra else 0)
+    pieces = []
+    while r0 < r1:
+        if mod_rows:
+            g = r0 // mod_rows
+            end = min(r1, (g + 1) * mod_rows)
+        else:
+            g, end = 0, r1
+        pieces.append((r0, end, g))
+        r0 = end
+    return pieces

@@ -91,11 +91,22 @@ typedef enum fp8q_status {
  *   cols        multiple of 8, 8 <= cols <= 32768 (3072 and 6144 take the tuned path)
  *   eps         >= 0 and finite (1e-6 on the pages)
  *   Aliasing: no output may overlap any input or the other output (FP8Q_ERR_ALIAS).
+ *   Value range: x must be finite with |x| < 2^56. The row sums (of x and of x^2) are kept in
+ *   fp32-range double-float arithmetic, so larger magnitudes may overflow them; rows holding
+ *   Inf or NaN, or values at or above 2^56, give unspecified y and q (no error is reported:
+ *   checking would cost a pass over the data). With eps = 0 a row whose squares all underflow
+ *   fp32 (|x| below about 1e-19) is also outside the contract.
  *   The row sums are formed error-free except for an fp32 sum of per-element rounding
  *   errors: the mean comes out exact on the workload rows and the variance within about
  *   2^-43 * (max|x| / sigma)^2 relative. Each normalised value is rounded to BF16 as the exact
  *   value would be, except when that value lies within about that relative distance of a
  *   BF16 rounding midpoint.
+ *   Row slices (one call per GPU or per piece of a larger tensor): the modulation row of data
+ *   row r is r / mod_rows counted from the call's own first row. A piece of rows [r0, r1)
+ *   of a larger tensor is therefore passed as x + r0*cols with mod_rows = 0 and scale/shift
+ *   pointing at the row of its modulation group, g = r0 / mod_rows, and every piece must lie
+ *   inside one group (split a slice at multiples of mod_rows); the binding's row_pieces()
+ *   makes such pieces.
  */
 fp8q_status fp8q_nss_fp8(void* y_bf16, uint8_t* q_e4m3, const void* x_bf16,
                          const void* scale_bf16, const void* shift_bf16, int64_t mod_rows,
@@ -116,6 +127,9 @@ fp8q_status fp8q_nss_fp8(void* y_bf16, uint8_t* q_e4m3, const void* x_bf16,
  *   bias         in  [cols] bf16 or NULL (no input bias)
  *   gate, scale, shift in [n_mod, cols] bf16 (m = r / mod_rows as above)
  *   Aliasing: residual_out may equal residual exactly; every other overlap is rejected.
+ *   Value range and row slices: as for fp8q_nss_fp8 (x, residual and the updated residual
+ *   finite with magnitudes below 2^56; pieces inside one modulation group, gate offset like
+ *   scale and shift).
  */
 fp8q_status fp8q_scale_residual_nss_fp8(void* residual_out, void* y_bf16, uint8_t* q_e4m3,
                                         const void* x_bf16, const void* residual_bf16,

@@ -110,9 +110,9 @@ def test_nss_shapes_and_ragged_rows(rows, cols, mod_rows):
     check_ln(yg, qg, yr, qr, 0.05, f"shape {rows}x{cols}/{mod_rows}")
 
 
-def test_nss_width_3072_one_warp_per_row():
-    """Above 48 rows per SM the width-3072 LayerNorm gives each warp a whole row (below, two
-    warps share one); a ragged row count and three modulation groups."""
+def test_nss_width_3072_many_rows_per_cta():
+    """50 rows per SM: each CTA of the width-3072 kernel refills its row ring more than once
+    (a ragged row count and three modulation groups, so CTAs are divided among groups)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     rows = 50 * sms + 37
     mod_rows = (rows + 2) // 3
@@ -123,11 +123,12 @@ def test_nss_width_3072_one_warp_per_row():
 
 
 def test_nss_kernel_choices_give_identical_bits():
-    """The row count picks the kernel (CTA per row up to 2 rows per SM; two warps per row with
-    16 or, from 16 rows per SM, 24 warps; one warp per row above 48 rows per SM). Across each
-    boundary the same leading rows must come out bit for bit the same."""
+    """The row count picks the kernel (CTA per row up to 2 rows per SM, the warp-specialised
+    kernel above) and, inside the latter, how many ring stages a CTA refills (21 stages: the
+    refill starts at 22 rows per CTA). Across each boundary the same leading rows must come
+    out bit for bit the same."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for n in (2 * sms, 16 * sms - 1, 48 * sms):
+    for n in (2 * sms, 21 * sms, 48 * sms):
         inp = W.nss_inputs(n + 1, 3072, seed=n, outlier_channels=30)
         a = run_nss({k: v[:n] if k == "x" else v for k, v in inp.items()}, 0.0625)
         b = run_nss(inp, 0.0625)
@@ -162,6 +163,114 @@ def test_nss_degenerate_rows():
     # constant row: n == 0 exactly, so y == shift bitwise
     yg, _ = run_nss(dict(x=x, scale=scale, shift=shift), 0.05)
     assert np.array_equal(yg[0], shift[0]) and np.array_equal(yg[1], shift[0])
+
+
+def _edge_rows(cols, rng):
+    """Rows at the edges of the documented value range (|x| < 2^56, finite): full rows near
+    2^55, one element just under 2^56, 2^50 and 2^-50 mixed, bf16 subnormals, values near
+    2^-60 (eps dominates), a constant 2^55 row, a large mean with a spread of a few bf16
+    steps."""
+    bf = lambda v: W.to_bf16_bits(torch.tensor(np.asarray(v, np.float32)))
+    z = rng.standard_normal(cols)
+    one = z.copy()
+    one[cols // 3] = 2.0 ** 55 * 1.9921875  # the largest bf16 below 2^56
+    sign = np.where(rng.random(cols) < 0.5, -1.0, 1.0)
+    mixed = np.where(rng.random(cols) < 0.5, 2.0 ** 50, 2.0 ** -50) * sign * (1 + rng.random(cols))
+    return np.stack([bf(z * 2.0 ** 53), bf(one), bf(mixed), bf(z * 1e-39), bf(z * 2.0 ** -60),
+                     bf(np.full(cols, 2.0 ** 55)), bf(2.0 ** 20 + z * 2.0 ** 14)])
+
+
+@pytest.mark.parametrize("cols", (3072, 6144))
+def test_nss_value_range_edges(cols):
+    """The edge rows alone (one CTA per row) and tiled among normal rows in a launch large
+    enough for the tuned kernels (width 3072: warp-specialised, 6144: two warps per row)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rng = np.random.default_rng(cols)
+    edges = _edge_rows(cols, rng)
+    g = torch.Generator().manual_seed(cols)
+    scale = W.normal_bf16((1, cols), 0.1, g)
+    shift = W.normal_bf16((1, cols), 0.1, g)
+    big = W.nss_inputs(2 * sms + 101, cols, seed=cols + 1)["x"]
+    big[::37][: len(edges) * 4] = np.tile(edges, (4, 1))[: big[::37].shape[0]]
+    for x in (edges, big):
+        for s in (0.05, 2.0 ** 50):
+            inp = dict(x=x, scale=scale, shift=shift)
+            yg, qg = run_nss(inp, s)
+            yr, qr = oracle.nss_fp8(x, scale, shift, s)
+            check_ln(yg, qg, yr, qr, s, f"value-range edges {x.shape[0]}x{cols} s={s}")
+
+
+def test_nss_row_pieces_reproduce_the_single_call():
+    """A FLUX.2-shaped launch (two modulation groups) cut for 3 and 8 ranks into pieces that
+    lie inside one group (each a call with mod_rows = 0 and its group's scale/shift rows):
+    the pieces together give the single call's outputs."""
+    c = W.CONFIGS["nss_flux"]
+    inp = W.config_inputs("nss_flux")
+    yr, qr = oracle.nss_fp8(inp["x"], inp["scale"], inp["shift"], c["input_scale"],
+                            mod_rows=c["mod_rows"])
+    for world in (3, 8):
+        yp = np.empty_like(yr)
+        qp = np.empty_like(qr)
+        for rank in range(world):
+            for r0, r1, grp in fq().row_pieces(inp["x"].shape[0], c["mod_rows"], world, rank):
+                piece = dict(x=inp["x"][r0:r1], scale=inp["scale"][grp:grp + 1],
+                             shift=inp["shift"][grp:grp + 1])
+                yp[r0:r1], qp[r0:r1] = run_nss(piece, c["input_scale"])
+        check_ln(yp, qp, yr, qr, c["input_scale"], f"row pieces for {world} ranks")
+
+
+def test_pdl_producer_consumer_chains_on_one_stream():
+    """Every launch allows programmatic dependent launch and every kernel waits for the
+    grids it depends on before its first global access. Chains on one stream with no
+    synchronisation in between, each consumer reading what the kernel just before it wrote
+    (the destinations hold stale values first, so reading too early shows):
+    bias_mul_add -> nss_fp8; scale_residual_nss_fp8 in place -> nss_fp8 on the updated
+    residual; nss_fp8 -> nss_fp8 on its y; a torch elementwise kernel -> nss_fp8; a torch
+    elementwise kernel -> token_cat_fp8."""
+    c = W.CONFIGS["scale_residual_qwen"]
+    r = W.config_inputs("scale_residual_qwen")
+    s = c["input_scale"]
+    x, res = G.dev_bf16(r["x"]), G.dev_bf16(r["residual"])
+    bias, gate = G.dev_bf16(r["bias"]), G.dev_bf16(r["gate"])
+    scale, shift = G.dev_bf16(r["scale"]), G.dev_bf16(r["shift"])
+    ds = G.dev_scale(s)
+    x1_ref = oracle.bias_mul_add(r["x"], r["bias"], r["gate"][0], r["residual"])
+    y1_ref, q1_ref = oracle.nss_fp8(x1_ref, r["scale"], r["shift"], s)
+    ro_ref, _, _ = oracle.scale_residual_nss_fp8(r["x"], r["residual"], r["bias"], r["gate"],
+                                                 r["scale"], r["shift"], s)
+    y2_ref, q2_ref = oracle.nss_fp8(ro_ref, r["scale"], r["shift"], s)
+    y3_ref, q3_ref = oracle.nss_fp8(y1_ref, r["scale"], r["shift"], s)
+    t = W.config_inputs("token_cat_flux")
+    tc = W.CONFIGS["token_cat_flux"]
+    qc_ref = oracle.token_cat_fp8(t["a"], t["m"], tc["input_scale"])
+    a_src, m = G.dev_bf16(t["a"]), G.dev_bf16(t["m"])
+    a = torch.zeros_like(a_src)
+    x_copy = torch.zeros_like(x)
+    for rep in range(3):
+        x1 = torch.zeros_like(x)
+        resid = res.clone()
+        torch.cuda.synchronize()
+        fq().bias_mul_add(x, bias, gate[0], res, y=x1)
+        y1, q1 = fq().nss_fp8(x1, scale, shift, ds)
+        fq().scale_residual_nss_fp8(x, resid, gate, scale, shift, ds, bias=bias,
+                                    residual_out=resid)
+        y2, q2 = fq().nss_fp8(resid, scale, shift, ds)
+        y3, q3 = fq().nss_fp8(y1, scale, shift, ds)
+        x_copy.zero_()
+        torch.mul(x1, 1, out=x_copy)  # an elementwise torch kernel as the producer
+        y4, q4 = fq().nss_fp8(x_copy, scale, shift, ds)
+        a.zero_()
+        torch.mul(a_src, 1, out=a)
+        qc = fq().token_cat_fp8(a, m, G.dev_scale(tc["input_scale"]))
+        torch.cuda.synchronize()
+        assert np.array_equal(G.host_u16(x1), x1_ref), f"rep {rep}: bias_mul_add"
+        assert np.array_equal(G.host_u16(resid), ro_ref), f"rep {rep}: in-place residual"
+        for yg, qg, yr_, qr_, what in ((y1, q1, y1_ref, q1_ref, "after bias_mul_add"),
+                                       (y2, q2, y2_ref, q2_ref, "after in-place residual"),
+                                       (y3, q3, y3_ref, q3_ref, "on the previous y"),
+                                       (y4, q4, y1_ref, q1_ref, "after a torch copy")):
+            check_ln(G.host_u16(yg), G.host_u8(qg), yr_, qr_, s, f"PDL chain {what} rep {rep}")
+        assert np.array_equal(G.host_u8(qc), qc_ref), f"rep {rep}: token_cat after a torch copy"
 
 
 def test_nss_eps_values():
