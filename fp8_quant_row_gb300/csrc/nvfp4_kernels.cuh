@@ -24,7 +24,6 @@
 namespace fp8q {
 
 constexpr int kFp4Threads = 256;
-constexpr int kFp4UnitsPerCta = 32;  // 8 warps x 4 units, each over the same 8 rows
 
 // 32-byte streaming load / store (sm_100+ 256-bit global accesses).
 __device__ __forceinline__ void ld_stream32(const void* p, uint32_t (&w)[8]) {
@@ -94,26 +93,38 @@ __device__ __forceinline__ void quant_group(const uint32_t (&w)[8], float out, u
 // after one shuffle the warp writes four whole sectors with one store instruction, and the
 // L2 never sees a partial-sector scale write. A CTA (8 warps) covers 32 consecutive units
 // of its 8 rows. Grid: x = unit blocks of a row, y = row groups (grid-stride).
+// Work items are warp-sized: (8-row group, 4 consecutive units), taken in order by the warps of
+// a persistent grid (item it of warp w of CTA b: it = b * 8 + w, then + 8 * gridDim.x). A warp
+// item covers four scale words of each of its 8 rows, which share 32-byte sectors of the
+// 128x4 tile (see the shuffle below). Items rather than CTAs are the unit of balance, so a
+// launch of a little more than one wave of CTAs (512 tokens: 768 CTA-sized blocks on 608
+// slots) spreads evenly over every warp instead of running a second, mostly empty wave.
 __global__ void __launch_bounds__(kFp4Threads) token_cat_nvfp4_kernel(
     uint8_t* __restrict__ q, uint8_t* __restrict__ sf, const uint16_t* __restrict__ a,
     int a_units, const uint16_t* __restrict__ m, int m_units,
     const float* __restrict__ global_scale, int64_t rows, int64_t rows_pad) {
   const int units = a_units + m_units;  // also the number of 4-group scale tiles per row
+  const int quads = (units + 3) / 4;    // warp items per 8-row group
+  const int64_t items = (rows_pad / 8) * quads;
   const int a_cols = a_units * 64, m_cols = m_units * 64;
   const int lane = threadIdx.x & 31;
   const int j = lane >> 2;                        // row of the group: line parity j & 1, band j >> 1
-  const int ku = blockIdx.x * kFp4UnitsPerCta + (threadIdx.x >> 5) * 4 + (lane & 3);
   // shuffle source for the sector layout: lane L stores word L & 7 of sector L >> 3, which
   // holds line parity (L & 7) >> 2 and band (L & 3)
   const int src_j = ((lane & 3) << 1) | ((lane >> 2) & 1);
   const int src = src_j * 4 + (lane >> 3);
-  const int st_ku = blockIdx.x * kFp4UnitsPerCta + (threadIdx.x >> 5) * 4 + (lane >> 3);
   wait_for_producers();
   const float g = __ldg(global_scale);
   const float inv6 = __frcp_rn(6.0f);
   const float inv_g = __frcp_rn(g);
+  constexpr int kWarps = kFp4Threads / 32;
 
-  for (int64_t grp = blockIdx.y; grp < rows_pad / 8; grp += gridDim.y) {
+  for (int64_t it = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); it < items;
+       it += int64_t(gridDim.x) * kWarps) {
+    const int64_t grp = it / quads;
+    const int uq = int(it - grp * quads);
+    const int ku = uq * 4 + (lane & 3);
+    const int st_ku = uq * 4 + (lane >> 3);
     const int64_t band = grp >> 4;
     const int t0 = int(grp & 15) * 2;  // even line of the band
     const int64_t r = band * 128 + (j >> 1) * 32 + t0 + (j & 1);

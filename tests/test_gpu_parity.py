@@ -448,7 +448,9 @@ def test_token_cat_nvfp4_flux_config_bit_exact():
 
 @pytest.mark.parametrize("rows,a_cols,m_cols", [(1, 6144, 18432), (17, 6144, 18432),
                                                 (129, 6144, 18432), (127, 64, 64),
-                                                (5, 64, 1024), (300, 128, 192)])
+                                                (5, 64, 1024), (300, 128, 192),
+                                                # the register-capped one-wave build
+                                                (512, 6144, 18432), (333, 6144, 18432)])
 def test_token_cat_nvfp4_shapes_and_padding(rows, a_cols, m_cols):
     inp = W.token_cat_inputs(rows, a_cols, m_cols, seed=rows + 7)
     for g in (60.0, 1.0, 358.4, 1e-3, 1e6):
