@@ -191,10 +191,16 @@ __device__ __forceinline__ bool mean_far_from_bf16_grid(float mu_hi) {
 // normalised value n = RN_bf16((x - mu) * rstd)
 // ------------------------------------------------------------------------------------------
 
-// Fast path: t = RN(RN(x - mu_hi) * r_hi + c). Its error is below 4 fp32 ulps of t plus the
-// absolute term bounded through t_small; the bf16 rounding of t is therefore certain unless
-// the low 16 bits of t are within kGuard of the midpoint pattern 0x8000, or |t| < t_small.
-constexpr uint32_t kGuard = 8;
+// Fast path: t = RN(RN(x - mu_hi) * r_hi + c), c = RN(-mu_lo * r_hi). Against the exact
+// (x - mu) r its error is below 2.5 fp32 ulps of t: the rounding of x - mu_hi and the
+// neglected r_lo each move it by at most 2^-24 |t| (under one ulp), the fused multiply-add
+// rounds once (half an ulp); c's rounding and the row statistics' relative error (about
+// 2^-34 on the workload rows, far below 2^-24 on any bf16 row) add a small fraction of an ulp,
+// and the absolute error terms are bounded through t_small. The bf16 rounding of t is
+// therefore certain unless the low 16 bits of t are within kGuard = 3 of the midpoint
+// pattern 0x8000 (otherwise t is at least 4 ulps from the midpoint), or |t| < t_small. The
+// QKV epilogue's fast value (within one ulp) uses the same test.
+constexpr uint32_t kGuard = 3;
 constexpr uint32_t kGuardAdd = ((kGuard - 0x8000u) & 0xFFFFu) << 16;
 constexpr uint32_t kGuardMax = (2u * kGuard) << 16;
 

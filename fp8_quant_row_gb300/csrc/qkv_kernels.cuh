@@ -23,7 +23,7 @@
 // ~2^-53 of the total). Accumulator offsets come off as exact integers of their ulps, which
 // the lanes of a head add as integers. 1/sqrt(mean + eps) is a double-float (~2^-45). The
 // fast path t = fma(p, r_hi, p r_lo), p = x w (exact), is within one fp32 ulp of the exact
-// value; only values whose low 16 bits lie within 8 of the BF16 midpoint pattern take the
+// value; only values whose low 16 bits lie within 3 of the BF16 midpoint pattern take the
 // exact path (TwoProduct + the tie broken by the low part).
 #pragma once
 
@@ -305,7 +305,7 @@ __device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], const uint8_t*
 }
 
 // Normalised words n = RN_bf16(x w r) for one packed word; sets `unsure` when the fast value
-// could round the other way (its low 16 bits lie within 8 of the BF16 midpoint pattern; the
+// could round the other way (its low 16 bits lie within 3 of the BF16 midpoint pattern; the
 // fast path is within one fp32 ulp of the exact value).
 __device__ __forceinline__ uint32_t norm_word(f2 p, f2 rh, f2 rl, bool& unsure) {
   const f2 t = fma2(p, rh, mul2(p, rl));
