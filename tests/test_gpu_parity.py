@@ -63,6 +63,7 @@ def run_nss(inp, input_scale, mod_rows=0, eps=1e-6):
                  mod_rows=mod_rows, eps=eps, y=y.tensor, q=q.tensor)
     torch.cuda.synchronize()
     assert y.intact() and q.intact(), "write outside an output buffer"
+    assert fq().device_error() == 0, "a bounded wait inside the kernel ran out"
     return G.host_u16(y.tensor), G.host_u8(q.tensor)
 
 
@@ -263,6 +264,7 @@ def test_pdl_producer_consumer_chains_on_one_stream():
         torch.mul(a_src, 1, out=a)
         qc = fq().token_cat_fp8(a, m, G.dev_scale(tc["input_scale"]))
         torch.cuda.synchronize()
+        assert fq().device_error() == 0, f"rep {rep}: a bounded wait inside a kernel ran out"
         assert np.array_equal(G.host_u16(x1), x1_ref), f"rep {rep}: bias_mul_add"
         assert np.array_equal(G.host_u16(resid), ro_ref), f"rep {rep}: in-place residual"
         for yg, qg, yr_, qr_, what in ((y1, q1, y1_ref, q1_ref, "after bias_mul_add"),
