@@ -22,9 +22,9 @@
 // the FastTwoSum error kept, and those second-level errors summed in fp32 (their rounding is
 // ~2^-53 of the total). Accumulator offsets come off as exact integers of their ulps, which
 // the lanes of a head add as integers. 1/sqrt(mean + eps) is a double-float (~2^-45). The
-// fast path t = fma(p, r_hi, p r_lo), p = x w (exact), is within one fp32 ulp of the exact
-// value; only values whose low 16 bits lie within 3 of the BF16 midpoint pattern take the
-// exact path (TwoProduct + the tie broken by the low part).
+// fast path (per-token kernel t = fma(p, r_hi, p r_lo), ring kernel t = RN(p r_hi); p = x w
+// exact) is within 1.5 fp32 ulps of the exact value; only values whose low 16 bits lie within 3
+// of the BF16 midpoint pattern take the exact path (TwoProduct + the tie broken by the low part).
 #pragma once
 
 #include "fp8q_device.cuh"
@@ -305,10 +305,12 @@ __device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], const uint8_t*
 }
 
 // Normalised words n = RN_bf16(x w r) for one packed word; sets `unsure` when the fast value
-// could round the other way (its low 16 bits lie within 3 of the BF16 midpoint pattern; the
-// fast path is within one fp32 ulp of the exact value).
+// could round the other way (its low 16 bits lie within 3 of the BF16 midpoint pattern). The
+// fast value RN(p r_hi) (p = x w exact) is within 1.5 fp32 ulps of the exact p (r_hi + r_lo):
+// half an ulp from its rounding, under one from the neglected r_lo (|r_lo| <= 2^-24 r_hi).
 __device__ __forceinline__ uint32_t norm_word(f2 p, f2 rh, f2 rl, bool& unsure) {
-  const f2 t = fma2(p, rh, mul2(p, rl));
+  (void)rl;
+  const f2 t = mul2(p, rh);
   unsure |= near_bf16_midpoint(f2_lo(t)) | near_bf16_midpoint(f2_hi(t));
   return pack_bf16x2(f2_lo(t), f2_hi(t));
 }
