@@ -9,10 +9,11 @@ inside every timed step). The other kernels of the path (scale-residual, bias_mu
 FLUX.2 width-6144 LayerNorm and token-cat) are timed the same way and reported under
 `kernels` with their own roofline figures.
 
-Timing: W warm-up steps, then K steps replayed from CUDA graphs on one stream and timed
-with CUDA events on that stream; the buffer sets rotate and together exceed 2x L2, so every
-launch reads its inputs from HBM. SM clocks are sampled with nvidia-smi during the timed
-region. Under torchrun each rank runs the same workload on its own GPU (independent
+Timing: W warm-up steps, then windows of exactly K steps replayed from CUDA graphs on one
+stream, each timed with CUDA events recorded as nodes of those graphs (before the first and
+after the last launch) and bracketed by a barrier and a device synchronisation; the headline
+is the median window. The buffer sets rotate and together exceed 2x L2, so every launch reads
+its inputs from HBM. SM clocks are sampled with nvidia-smi during the timed region. Under torchrun each rank runs the same workload on its own GPU (independent
 replicas, weak scaling; the only collective is the timing barrier / max-reduce).
 
   python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
@@ -419,12 +420,30 @@ def extra_cases(torch, lib, l2, only=None):
     return {k: f for k, f in builders.items() if only is None or k == only}
 
 
-def capture(torch, case: Case, count: int, start: int):
+def capture(torch, case: Case, count: int, start: int, ev_first=None, ev_last=None):
+    """A graph of `count` launches; ev_first / ev_last (events created with external=True)
+    are recorded as graph nodes before the first and after the last launch, so a window's
+    time is the device time of exactly its launches, without the host's graph-launch latency
+    in front of them."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
+        if ev_first is not None:
+            ev_first.record()
         for i in range(count):
             case.launch(start + i)
+        if ev_last is not None:
+            ev_last.record()
     return g
+
+
+def graph_events(torch):
+    """Timing events that become event-record nodes when recorded during capture, or None
+    where torch lacks them (then the events are recorded on the stream around the replay)."""
+    try:
+        return (torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
+    except TypeError:
+        return None
 
 
 def windows_needed(first_window_ms: float, repeats: int, min_region_s: float) -> int:
@@ -444,19 +463,26 @@ def time_case(torch, case: Case, steps: int, warmup: int, use_graph=True, barrie
         case.launch(i)
     torch.cuda.synchronize()
     graphs = []
+    in_graph = graph_events(torch) if use_graph else None
     if use_graph:
         # chunks of GRAPH_CHUNK launches (the last one may be shorter); every chunk starts on
         # a set index that continues the rotation
         done = 0
         while done < steps:
             cnt = min(GRAPH_CHUNK, steps - done)
-            graphs.append(capture(torch, case, cnt, warmup + done))
+            first = in_graph[0] if in_graph and done == 0 else None
+            last = in_graph[1] if in_graph and done + cnt >= steps else None
+            graphs.append(capture(torch, case, cnt, warmup + done, first, last))
             done += cnt
         # one untimed replay to page everything in
-        graphs[0].replay()
+        for g in graphs:
+            g.replay()
         torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
+    if in_graph:
+        ev0, ev1 = in_graph
+    else:
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
     windows = []
     t0 = t1 = None
     while True:
@@ -465,14 +491,16 @@ def time_case(torch, case: Case, steps: int, warmup: int, use_graph=True, barrie
         torch.cuda.synchronize()
         if t0 is None:
             t0 = time.time()
-        ev0.record()
+        if not in_graph:
+            ev0.record()
         if use_graph:
             for g in graphs:
                 g.replay()
         else:
             for i in range(steps):
                 case.launch(warmup + i)
-        ev1.record()
+        if not in_graph:
+            ev1.record()
         torch.cuda.synchronize()
         t1 = time.time()
         windows.append(ev0.elapsed_time(ev1))
@@ -688,9 +716,11 @@ def run_ours(args):
                    "l2": f"{main.n_sets} rotating buffer sets, "
                          f"{main.n_sets * main.alg_bytes / 2**20:.0f} MiB > 2x L2 "
                          f"({l2 / 2**20:.0f} MiB): inputs are cold in L2 at every launch",
-                   "timing": "CUDA events on the launch stream around K launches replayed "
-                             "from CUDA graphs" if not args.no_graph else
-                             "CUDA events around K direct launches",
+                   "timing": "CUDA events recorded as nodes of the CUDA graphs that hold the K "
+                             "launches (before the first, after the last), so a window is the "
+                             "device time of exactly its K launches; the median window of "
+                             "several, each bracketed by a barrier and device synchronisation"
+                             if not args.no_graph else "CUDA events around K direct launches",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline_entry(main, ms_step, peak, peak_src),
         "gpu_launches": args.steps,
