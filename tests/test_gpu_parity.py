@@ -123,6 +123,20 @@ def test_nss_width_3072_many_rows_per_cta():
     check_ln(yg, qg, yr, qr, 0.0625, f"one warp per row, {rows} rows")
 
 
+def test_nss_more_modulation_groups_than_sms():
+    """Every CTA of the tuned kernels serves one modulation group, so a launch with more
+    groups than SMs (here one scale/shift row per data row) falls back to the CTA-per-row
+    kernel; it must still match the oracle, and so must a launch with exactly one group per
+    SM's worth of rows."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for rows, mod_rows in ((2 * sms + 96, 1), (3 * sms, 3), (sms * 10 + 7, 10)):
+        n_mod = (rows + mod_rows - 1) // mod_rows
+        inp = W.nss_inputs(rows, 3072, seed=rows + mod_rows, n_mod=n_mod, outlier_channels=30)
+        yg, qg = run_nss(inp, 0.05, mod_rows=mod_rows)
+        yr, qr = oracle.nss_fp8(inp["x"], inp["scale"], inp["shift"], 0.05, mod_rows=mod_rows)
+        check_ln(yg, qg, yr, qr, 0.05, f"{rows} rows, {n_mod} modulation groups")
+
+
 def test_nss_kernel_choices_give_identical_bits():
     """The row count picks the kernel (CTA per row up to 2 rows per SM, the warp-specialised
     kernel above) and, inside the latter, how many ring stages a CTA refills (21 stages: the
