@@ -211,8 +211,7 @@ fp8q_status launch_tuned(const fp8q::NssParams& p, const DeviceInfo& dev, int64_
 }
 
 // Warp-specialised kernel: one CTA per SM (never more CTAs than rows), each owning a block
-// of rows; the ring holds as many row stages as shared memory allows, rounded down to a
-// multiple of the stage quantum (see nss_ws_kernels.cuh) and no more than the CTA's rows need.
+// of rows that it streams through a ring of WsLayout::kStages row stages.
 constexpr int kWsDepth = 1 << 30;  // rows in flight per CTA (no limit beyond the ring)
 
 template <int C, int NS, int NO>
@@ -223,18 +222,13 @@ fp8q_status launch_ws(const fp8q::NssParams& p, const DeviceInfo& dev, int64_t n
   *launched = false;
   int64_t grid = std::min<int64_t>(dev.sms, p.rows);
   if (n_mod > grid) return FP8Q_OK;  // every CTA must sit inside one modulation group
-  const int64_t rows_per_cta = (p.rows + grid - 1) / grid + 1;  // group splits add one
-  const int q = L::kStageQuantum;
-  int64_t stages = int64_t(size_t(dev.smem_optin) / L::kStageBytes) / q * q;
-  stages = std::min<int64_t>(stages, (rows_per_cta + q - 1) / q * q);
-  if (stages < q) return FP8Q_OK;
-  const size_t smem = L::smem_bytes(int(stages));
+  if (L::kSmemBytes > size_t(dev.smem_optin)) return FP8Q_OK;
   int bps = 0;
-  fp8q_status st = blocks_per_sm(reinterpret_cast<const void*>(fn), L::kThreads, smem, &bps);
+  fp8q_status st = blocks_per_sm(reinterpret_cast<const void*>(fn), L::kThreads, L::kSmemBytes, &bps);
   if (st != FP8Q_OK) return st;
   if (bps <= 0) return FP8Q_OK;
   *launched = true;
-  return launch(fn, dim3(unsigned(grid)), dim3(L::kThreads), smem, stream, p, n_mod, int(stages),
+  return launch(fn, dim3(unsigned(grid)), dim3(L::kThreads), L::kSmemBytes, stream, p, n_mod,
                 kWsDepth);
 }
 

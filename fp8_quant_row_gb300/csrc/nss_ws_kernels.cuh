@@ -7,25 +7,29 @@
 // E4M3(RN(y * RN(1/input_scale))). What differs is how a CTA moves rows through the SM:
 //
 //   producer warp   one lane issues one bulk copy (cp.async.bulk, TMA) per row into a ring of
-//                   S row stages in shared memory; stage s's `full` mbarrier completes when the
-//                   row has landed. A stage is refilled once its `empty` mbarrier completes,
-//                   and at most `depth` rows are in flight at a time.
-//   statistics      NS warps; warp i takes rows i, i + NS, ...: it waits for the row, forms the
-//   warps           error-free row sums and the row constants once per row, stores them in the
-//                   stage's constant slot and arrives on the stage's `done` mbarrier.
-//   output warps    the row is cut into parts of 768 columns; NO warps per part take rows
-//                   idx, idx + NO, ... of their part. Each keeps RN(1 + scale) and shift of its
-//                   768 columns in registers for the whole launch, waits for `done`, writes
-//                   y and q of its part and arrives on `empty`.
+//                   kStages row stages in shared memory; stage s's `full` mbarrier completes
+//                   when the row has landed. A stage is refilled once its `empty` mbarrier
+//                   completes, and at most `depth` rows are in flight at a time.
+//   statistics      NS warps; each claims the CTA's next row in order (a shared counter), waits
+//   warps           for it, forms the error-free row sums and the row constants once per row,
+//                   stores them in the stage's constant slot and arrives on its `done` mbarrier.
+//   output warps    the row is cut into parts of 768 columns; NO warps per part claim the next
+//                   row of their part in order (a counter per part). Each keeps RN(1 + scale)
+//                   and shift of its 768 columns in registers for the whole launch, waits for
+//                   `done`, writes y and q of its part and arrives on `empty`.
 //
 // The constants of a row are formed once (not once per warp that touches the row), the
 // statistics (FMA-pipe heavy) and output (ALU heavy) phases of different rows run at the same
-// time on different warps, and no consumer warp ever issues a load from global memory.
+// time on different warps, no consumer warp ever issues a load from global memory, and a row
+// goes to whichever warp of a role is free first (a static row-to-warp assignment made rows
+// wait for one busy warp while others idled).
 //
-// mbarrier phases: stage s holds rows s, s + S, s + 2S, ...; row k is the (k / S)-th use of
-// its stage and waits for the phase of that parity. S is a multiple of NS and of NO, so the
-// warp that waits for use u of a stage is the warp that consumed use u - 1: no waiter can
-// run a phase ahead and mistake an older phase of the same parity for its own.
+// mbarrier phases: stage s = k % kStages holds rows s, s + kStages, ...; row k is the
+// (k / kStages)-th use of its stage and waits for the phase of that parity. Before a stage's
+// second and later uses the waiter first checks the stage's row word, which the producer
+// writes just before it issues the copy (bounded wait): once it holds k, the stage's previous
+// use has been released, so every earlier phase of its barriers has completed and the parity
+// cannot be mistaken for an older phase's.
 //
 // Every wait is bounded (kWaitLimitCycles); a wait that runs out records kDevErrWaitTimeout
 // in the device error word and the warp stops taking rows. The producer finally waits
@@ -35,8 +39,6 @@
 #include "nss_kernels.cuh"
 
 namespace fp8q {
-
-constexpr int ws_gcd(int a, int b) { return b == 0 ? a : ws_gcd(b, a % b); }
 
 constexpr int kWsPartCols = 768;                  // columns of one output part
 constexpr int kWsPartChunks = kWsPartCols / 256;  // 16-byte chunks per lane per part (3)
@@ -50,10 +52,13 @@ struct WsLayout {
   static constexpr int kWarps = NS + kParts * NO + 1;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kProducerWarp = kWarps - 1;
-  static constexpr int kStageQuantum = NS * NO / ws_gcd(NS, NO);  // S must be a multiple
-  // per stage: the row, two float4 of row constants, three mbarriers
-  static constexpr size_t kStageBytes = size_t(kRowBytes) + 32 + 24;
-  static constexpr size_t smem_bytes(int stages) { return size_t(stages) * kStageBytes; }
+  static constexpr int kLogStages = 5;
+  static constexpr int kStages = 1 << kLogStages;  // deeper than NS and NO (see the header)
+  static_assert(kStages > NS && kStages > NO, "ring too shallow for the claiming argument");
+  // per stage: the row, two float4 of row constants, three mbarriers, the row word; then the
+  // claim counters (statistics, one per output part)
+  static constexpr size_t kStageBytes = size_t(kRowBytes) + 32 + 24 + 4;
+  static constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 16 * ((kParts + 4) / 4);
 };
 
 // Row constants of the row held in `stage` (this lane's chunks at stage[j * 32]), read from
@@ -157,17 +162,54 @@ __device__ __forceinline__ void ws_part_outputs(const uint4* xs, const f2 (&ops)
   }
 }
 
+// The next index of a shared counter for the whole warp (lane 0 increments, all lanes get it).
+__device__ __forceinline__ int ws_claim(int* ctr) {
+  int k = 0;
+  if ((threadIdx.x & 31) == 0) k = atomicAdd(ctr, 1);
+  return __shfl_sync(0xffffffffu, k, 0);
+}
+
+// The stage's row word: written with release semantics by the producer once the stage's
+// previous use has been released, read with acquire semantics by the consumers.
+__device__ __forceinline__ void ws_set_row(int* rowid, int k) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(rowid)), "r"(k)
+               : "memory");
+}
+__device__ __forceinline__ int ws_get_row(const int* rowid) {
+  int k;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(k) : "r"(smem_addr(rowid))
+               : "memory");
+  return k;
+}
+
+// Wait for phase u of `bar` for row k in stage s. From the second use of a stage on, first
+// (bounded) until the producer has written k into the stage's row word.
+__device__ __forceinline__ bool ws_wait_row(uint64_t* bar, const int* rowid, int s, int k,
+                                            int u) {
+  if (u > 0 && ws_get_row(rowid + s) != k) {
+    const long long t0 = clock64();
+    while (ws_get_row(rowid + s) != k) {
+      if (clock64() - t0 > kWaitLimitCycles) return false;
+      __nanosleep(100);
+    }
+  }
+  return mbar_wait(bar, u & 1);
+}
+
 template <int C, int NS, int NO>
 __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
-    nss_ws_kernel(const NssParams p, const int64_t n_mod, const int S, const int depth) {
+    nss_ws_kernel(const NssParams p, const int64_t n_mod, const int depth) {
   using L = WsLayout<C, NS, NO>;
   constexpr int P = L::kParts;
+  constexpr int S = L::kStages;
   extern __shared__ __align__(128) unsigned char ws_smem[];
   unsigned char* ring = ws_smem;
   float4* kslot = reinterpret_cast<float4*>(ws_smem + size_t(S) * L::kRowBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(kslot + 2 * S);
   uint64_t* done = full + S;
   uint64_t* empty = done + S;
+  int* rowid = reinterpret_cast<int*>(empty + S);
+  int* next_stats = rowid + S;  // then one counter per output part
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const RowBlock blk = cta_rows(p.rows, p.mod_rows, n_mod, blockIdx.x, gridDim.x);
@@ -178,7 +220,9 @@ __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
       mbar_init(full + s, 1);
       mbar_init(done + s, 1);
       mbar_init(empty + s, P);
+      rowid[s] = -1;
     }
+    for (int c = 0; c <= P; ++c) next_stats[c] = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -204,6 +248,7 @@ __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
             break;
           }
         }
+        ws_set_row(rowid + s, k);
         mbar_arrive_expect_tx(full + s, L::kRowBytes);
         bulk_load(ring + size_t(s) * L::kRowBytes, src + size_t(k) * L::kRowBytes, L::kRowBytes,
                   full + s);
@@ -227,9 +272,9 @@ __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
     // statistics warp
     const float colsf = float(C);
     const float rcols = __frcp_rn(colsf);
-    // stage s = k % S and use u = k / S, advanced without division (NS <= S)
-    for (int k = warp, s = warp, u = 0; k < n; k += NS) {
-      if (!mbar_wait(full + s, u & 1)) {
+    for (int k = ws_claim(next_stats); k < n; k = ws_claim(next_stats)) {
+      const int s = k & (S - 1), u = k >> L::kLogStages;
+      if (!ws_wait_row(full + s, rowid, s, k, u)) {
         report_device_error(kDevErrWaitTimeout);
         break;
       }
@@ -241,17 +286,12 @@ __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
             make_float4(kc.c, mean_far_from_bf16_grid(kc.mu_hi) ? 0.0f : kc.t_small, 0.0f, 0.0f);
         mbar_arrive(done + s);
       }
-      if ((s += NS) >= S) {
-        s -= S;
-        ++u;
-      }
     }
     return;
   }
 
-  // output warp: part `part` of rows idx, idx + NO, ...
-  const int o = warp - NS;
-  const int part = o % P, idx = o / P;
+  // output warp: part `part` of the rows it claims
+  const int part = (warp - NS) % P;
   const size_t col0 = size_t(part) * kWsPartCols;
   f2 ops[kWsPartChunks][4], sh[kWsPartChunks][4];
   {
@@ -271,9 +311,11 @@ __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
   }
   const float inv = __frcp_rn(__ldg(p.input_scale));
   const f2 inv2 = f2_make(inv, inv);
-  for (int k = idx, s = idx, u = 0; k < n; k += NO) {
-    // `full` first: it orders this wait after the stage's previous use (see the header)
-    if (!mbar_wait(full + s, u & 1) || !mbar_wait(done + s, u & 1)) {
+  int* const next_row = next_stats + 1 + part;
+  for (int k = ws_claim(next_row); k < n; k = ws_claim(next_row)) {
+    const int s = k & (S - 1), u = k >> L::kLogStages;
+    // `full` first: the stage's row word and the row's landing, then its constants
+    if (!ws_wait_row(full + s, rowid, s, k, u) || !mbar_wait(done + s, u & 1)) {
       report_device_error(kDevErrWaitTimeout);
       break;
     }
@@ -293,10 +335,6 @@ __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
     ws_part_outputs(xs, ops, sh, kc, inv2, yr, qr);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + s);
-    if ((s += NO) >= S) {
-      s -= S;
-      ++u;
-    }
   }
 }
 
