@@ -563,19 +563,21 @@ fp8q_status fp8q_qkv_epilogue(void* joint_q, void* joint_k, void* joint_v,
     dstp[i]->eps = st[i]->eps;
   }
   p.heads = int(heads);
-  if (heads <= fp8q::kQkvRingMaxHeads) {
-    // per-warp item pipelines; two or more CTAs per SM
-    const size_t smem = fp8q::kQkvWeightBytes +
-                        size_t(fp8q::kQkvRingWarps) * fp8q::kQkvDepth * fp8q::kQkvSlotBytes;
-    auto* fn = fp8q::qkv_ring_kernel;
-    int bps = 0;
-    stt = blocks_per_sm(reinterpret_cast<const void*>(fn), fp8q::kQkvRingWarps * 32, smem, &bps);
-    if (stt != FP8Q_OK) return stt;
-    if (bps > 0) {
-      const int64_t items = total * 3 * ((heads + 7) / 8);
-      const int64_t need = (items + fp8q::kQkvRingWarps - 1) / fp8q::kQkvRingWarps;
-      const int64_t grid = std::min<int64_t>(need, int64_t(dev->sms) * bps);
-      return launch(fn, dim3(unsigned(grid)), dim3(fp8q::kQkvRingWarps * 32), smem, stream, p);
+  if (heads <= fp8q::kQkvMaxWsHeads) {
+    // warp-specialised: one CTA per SM (never more CTAs than tokens), a ring of whole tokens
+    const size_t per_stage = fp8q::qws_stage_bytes(int(heads)) + 20;
+    const int64_t fit = (int64_t(dev->smem_optin) - fp8q::kQkvWeightBytes - 16) / int64_t(per_stage);
+    const int stages = int(std::min<int64_t>(fit, fp8q::kQwsMaxStages));
+    if (stages >= 2) {
+      const size_t smem = fp8q::qws_smem_bytes(int(heads), stages);
+      auto* fn = fp8q::qkv_ws_kernel;
+      int bps = 0;
+      stt = blocks_per_sm(reinterpret_cast<const void*>(fn), fp8q::kQwsThreads, smem, &bps);
+      if (stt != FP8Q_OK) return stt;
+      if (bps > 0) {
+        const int64_t grid = std::min<int64_t>(total, dev->sms);
+        return launch(fn, dim3(unsigned(grid)), dim3(fp8q::kQwsThreads), smem, stream, p, stages);
+      }
     }
   }
   const unsigned gx = unsigned(total < 0x7FFFFFFF ? total : 0x7FFFFFFF);

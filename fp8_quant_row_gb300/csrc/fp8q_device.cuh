@@ -428,6 +428,62 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
       : "memory");
 }
 
+// One bulk copy shared -> global (TMA, bulk-group completion), its commit, and the waits for
+// the committed groups: `.read` returns once at most N groups still read shared memory, the
+// plain form once at most N groups are incomplete. Both addresses 16-byte aligned, size a
+// multiple of 16.
+__device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               ::"l"(gmem_dst), "r"(smem_addr(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// The next index of a shared counter for the whole warp (lane 0 increments, all lanes get it).
+__device__ __forceinline__ int ws_claim(int* ctr) {
+  int k = 0;
+  if ((threadIdx.x & 31) == 0) k = atomicAdd(ctr, 1);
+  return __shfl_sync(0xffffffffu, k, 0);
+}
+
+// The stage's row word: written with release semantics by the producer once the stage's
+// previous use has been released, read with acquire semantics by the consumers.
+__device__ __forceinline__ void ws_set_row(int* rowid, int k) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(rowid)), "r"(k)
+               : "memory");
+}
+__device__ __forceinline__ int ws_get_row(const int* rowid) {
+  int k;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(k) : "r"(smem_addr(rowid))
+               : "memory");
+  return k;
+}
+
+// Wait for phase u of `bar` for row k in stage s. From the second use of a stage on, first
+// (bounded) until the producer has written k into the stage's row word.
+__device__ __forceinline__ bool ws_wait_row(uint64_t* bar, const int* rowid, int s, int k,
+                                            int u) {
+  if (u > 0 && ws_get_row(rowid + s) != k) {
+    const long long t0 = clock64();
+    while (ws_get_row(rowid + s) != k) {
+      if (clock64() - t0 > kWaitLimitCycles) return false;
+      __nanosleep(100);
+    }
+  }
+  return mbar_wait(bar, u & 1);
+}
+
+
 // Four E4M3 codes E4M3(RN(y * inv)) of two bf16 pairs, as one 32-bit word (y0 low pair in
 // bytes 0-1, y1 in bytes 2-3): two packed multiplies, two conversions, one byte permute.
 __device__ __forceinline__ uint32_t quant4(uint32_t y0, uint32_t y1, unsigned long long inv2) {

@@ -162,40 +162,6 @@ __device__ __forceinline__ void ws_part_outputs(const uint4* xs, const f2 (&ops)
   }
 }
 
-// The next index of a shared counter for the whole warp (lane 0 increments, all lanes get it).
-__device__ __forceinline__ int ws_claim(int* ctr) {
-  int k = 0;
-  if ((threadIdx.x & 31) == 0) k = atomicAdd(ctr, 1);
-  return __shfl_sync(0xffffffffu, k, 0);
-}
-
-// The stage's row word: written with release semantics by the producer once the stage's
-// previous use has been released, read with acquire semantics by the consumers.
-__device__ __forceinline__ void ws_set_row(int* rowid, int k) {
-  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(rowid)), "r"(k)
-               : "memory");
-}
-__device__ __forceinline__ int ws_get_row(const int* rowid) {
-  int k;
-  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(k) : "r"(smem_addr(rowid))
-               : "memory");
-  return k;
-}
-
-// Wait for phase u of `bar` for row k in stage s. From the second use of a stage on, first
-// (bounded) until the producer has written k into the stage's row word.
-__device__ __forceinline__ bool ws_wait_row(uint64_t* bar, const int* rowid, int s, int k,
-                                            int u) {
-  if (u > 0 && ws_get_row(rowid + s) != k) {
-    const long long t0 = clock64();
-    while (ws_get_row(rowid + s) != k) {
-      if (clock64() - t0 > kWaitLimitCycles) return false;
-      __nanosleep(100);
-    }
-  }
-  return mbar_wait(bar, u & 1);
-}
-
 template <int C, int NS, int NO>
 __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
     nss_ws_kernel(const NssParams p, const int64_t n_mod, const int depth) {

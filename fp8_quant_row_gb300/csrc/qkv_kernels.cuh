@@ -9,10 +9,11 @@
 //   V:     copied,
 // written to joint [text tokens + image tokens, heads, 128] buffers, text first.
 //
-// Two kernels: qkv_ring_kernel (up to 64 heads; per-warp cp.async pipelines, four lanes per
-// head, described below) and qkv_epilogue_kernel (any head count: one CTA per joint token,
-// 6 warps, two per kind; 8 lanes per head with one 32-byte load each, so a lane's 8 packed BF16
-// words are exactly its 8 RoPE pairs; a Q/K warp loads all its heads before computing any).
+// Two kernels: qkv_ws_kernel (up to 64 heads; warp-specialised, whole tokens streamed through
+// a shared-memory ring by bulk copies, four lanes per head, described below) and
+// qkv_epilogue_kernel (any head count: one CTA per joint token, 6 warps, two per kind; 8 lanes
+// per head with one 32-byte load each, so a lane's 8 packed BF16 words are exactly its 8 RoPE
+// pairs; a Q/K warp loads all its heads before computing any).
 //
 // Exactness of n: sum(x^2) per head is formed without rounding error that matters. Squares
 // of BF16 values are exact in fp32. They are accumulated from an offset K2 = 2^(2E+9) >= 128
@@ -22,9 +23,10 @@
 // the FastTwoSum error kept, and those second-level errors summed in fp32 (their rounding is
 // ~2^-53 of the total). Accumulator offsets come off as exact integers of their ulps, which
 // the lanes of a head add as integers. 1/sqrt(mean + eps) is a double-float (~2^-45). The
-// fast path (per-token kernel t = fma(p, r_hi, p r_lo), ring kernel t = RN(p r_hi); p = x w
-// exact) is within 1.5 fp32 ulps of the exact value; only values whose low 16 bits lie within 3
-// of the BF16 midpoint pattern take the exact path (TwoProduct + the tie broken by the low part).
+// fast path (per-token kernel t = fma(p, r_hi, p r_lo), warp-specialised kernel t = RN(p r_hi);
+// p = x w exact) is within 1.5 fp32 ulps of the exact value; only values whose low 16 bits lie
+// within 3 of the BF16 midpoint pattern take the exact path (TwoProduct + the tie broken by the
+// low part).
 #pragma once
 
 #include "fp8q_device.cuh"
@@ -231,21 +233,11 @@ __global__ void __launch_bounds__(kQkvWarps * 32, kQkvMinCtas) qkv_epilogue_kern
 }
 
 // ------------------------------------------------------------------------------------------
-// Ring kernel (heads <= 64): persistent CTAs stream whole tokens through a cp.async ring
+// helpers of the warp-specialised kernel
 // ------------------------------------------------------------------------------------------
-//
-// Four lanes per head, 32 values (16 packed words, 16 RoPE pairs) per lane, eight heads per
-// warp: the per-head work (reductions, double-float constants) is shared by 32 values.
-// Shared memory: the four RMSNorm weights (text q, k, image q, k; planar), then per warp
-// `kQkvDepth` slots. q, k, the weights and cos/sin are stored in four planes: 16-byte chunk j
-// of every 64-byte lane segment goes to plane j, so a warp's 16-byte loads of one plane are
-// contiguous (no bank conflicts); v is stored as is.
-constexpr int kQkvRingWarps = 8;
-constexpr int kQkvRingMaxHeads = 64;
 
-__device__ __forceinline__ void st_global16(void* p, float4 v) {
-  __stcs(reinterpret_cast<float4*>(p), v);
-}
+constexpr int kQkvMaxWsHeads = 64;     // the warp-specialised kernel's head limit
+constexpr int kQkvWeightBytes = 2048;  // four fp32 RMSNorm weight vectors
 
 __device__ __forceinline__ void lds_words4(const uint8_t* p, uint32_t* w) {
   const float4 v = lds128(reinterpret_cast<const float4*>(p));
@@ -255,14 +247,67 @@ __device__ __forceinline__ void lds_words4(const uint8_t* p, uint32_t* w) {
   w[3] = __float_as_uint(v.w);
 }
 
-// 1 / sqrt(sum(x^2) / 128 + eps) for the head held by this lane's group of 4 lanes (32 values
-// each), with the same exact accumulation as head_rrms; also returns p = x * weight (exact),
-// the weight pairs read as fp32 from shared memory, so each value is unpacked once.
-__device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], const uint8_t* wv, float eps,
-                                         f2 (&p)[16]) {
-  uint32_t m = absmax_bf16x2(w[0], w[1]);
+// ------------------------------------------------------------------------------------------
+// Warp-specialised kernel (heads <= 64): one CTA per SM streams whole tokens through a ring
+// ------------------------------------------------------------------------------------------
+//
+// A CTA owns a contiguous block of joint tokens (text first) and moves every token through a
+// ring of S stages in shared memory. A stage holds the token's q, k and v rows (heads x 256 B
+// each) and its cos/sin row (512 B), brought by four bulk copies (cp.async.bulk, TMA) that
+// complete on the stage's `full` mbarrier.
+//   producer warp  one lane issues the copies and refills a stage once its `empty` mbarrier
+//                  completes;
+//   V warp         one lane writes each token's v row back out with one bulk store from
+//                  shared memory (no register traffic) and releases the stage once the store
+//                  has read it;
+//   Q/K warps      claim units (token, Q or K, block of eight heads) in order from a shared
+//                  counter, normalise and rotate their heads, store the results directly and
+//                  arrive on `empty`.
+// Four lanes per head, 32 values per lane: lane q of a head holds the 16-byte chunks
+// c = q + 4 (j ^ o), j = 0..3, o the parity of the head within the block, so that one
+// 16-byte load of chunk index j by the warp reads 64 contiguous bytes per head and the eight
+// heads split evenly over the two halves of the banks (no conflicts). Values 8c .. 8c + 7 of
+// chunk c are RoPE pairs 4c .. 4c + 3.
+// mbarrier phases: stage s = k % S holds tokens s, s + S, ...; token k waits for the phase of
+// parity (k / S) & 1. The producer writes k into the stage's row word (release) before it
+// issues the copies, and a Q/K warp that claims a later use of the stage first waits for that
+// word, so it cannot take an older phase of the same parity for its own. The V warp and the
+// producer take the stage's uses in order. Every wait is bounded; a wait that runs out records
+// the device error and the warp stops.
+constexpr int kQwsQkWarps = 12;                  // Q/K warps per CTA
+constexpr int kQwsVWarp = kQwsQkWarps;           // then the V warp
+constexpr int kQwsProducerWarp = kQwsQkWarps + 1;
+constexpr int kQwsThreads = (kQwsQkWarps + 2) * 32;
+constexpr int kQwsMaxStages = 32;
+
+// Dynamic shared memory of the warp-specialised kernel: weights, S stages, then per stage two
+// mbarriers and the row word, and the unit counter.
+__host__ __device__ constexpr size_t qws_stage_bytes(int heads) {
+  return size_t(3) * heads * 256 + 512;
+}
+__host__ __device__ constexpr size_t qws_smem_bytes(int heads, int stages) {
+  return kQkvWeightBytes + size_t(stages) * (qws_stage_bytes(heads) + 20) + 16;
+}
+
+// RMSNorm + interleaved RoPE of the 16 words this lane holds, written to `dst` (the head's
+// output row). xs: the head's 256 bytes in the stage; wt: the 128 fp32 weights; cs: the
+// stage's cos (64 fp32) and sin (64 fp32) row; cidx: the lane's four chunk indices.
+__device__ __forceinline__ void qws_head(const uint8_t* xs, const float* wt, const float* cs,
+                                         float eps, const int (&cidx)[4], bool live,
+                                         uint16_t* dst) {
+  uint32_t x[16];
 #pragma unroll
-  for (int i = 2; i < 16; ++i) m = absmax_bf16x2(m, w[i]);
+  for (int j = 0; j < 4; ++j) {
+    if (live) {
+      lds_words4(xs + cidx[j] * 16, x + 4 * j);
+    } else {
+      x[4 * j] = x[4 * j + 1] = x[4 * j + 2] = x[4 * j + 3] = 0u;
+    }
+  }
+  // sum of squares (exact accumulation, as head_rrms) and p = x w (exact)
+  uint32_t m = absmax_bf16x2(x[0], x[1]);
+#pragma unroll
+  for (int i = 2; i < 16; ++i) m = absmax_bf16x2(m, x[i]);
   uint32_t mx = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
   mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
   mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
@@ -270,219 +315,200 @@ __device__ __forceinline__ dd head_rrms4(const uint32_t (&w)[16], const uint8_t*
   const float K2 = exp2i(2 * E + 9);
   const float K3 = 1.5f * exp2i(2 * E - 9);  // 48 u, u = 2^(2E - 14)
   f2 S = f2_make(K2, K2), R = f2_make(K3, K3), T = f2_make(0.0f, 0.0f);
+  f2 p[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const f2 v = bf2_to_f2(w[i]);
-    if ((i & 1) == 0) {
-      const float4 w4 = lds128(reinterpret_cast<const float4*>(wv + (i >> 1) * 64));
-      p[i] = mul2(v, f2_make(w4.x, w4.y));
-      p[i + 1] = mul2(bf2_to_f2(w[i + 1]), f2_make(w4.z, w4.w));
+  for (int j = 0; j < 4; ++j) {
+    const float4 w0 = lds128(reinterpret_cast<const float4*>(wt + 8 * cidx[j]));
+    const float4 w1 = lds128(reinterpret_cast<const float4*>(wt + 8 * cidx[j] + 4));
+    const f2 wp[4] = {f2_make(w0.x, w0.y), f2_make(w0.z, w0.w), f2_make(w1.x, w1.y),
+                      f2_make(w1.z, w1.w)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const f2 v = bf2_to_f2(x[4 * j + i]);
+      p[4 * j + i] = mul2(v, wp[i]);
+      const f2 sn = fma2(v, v, S);
+      const f2 e = fma2(v, v, sub2(S, sn));  // exact error of sn
+      S = sn;
+      const f2 r = add2(R, e);
+      T = add2(T, sub2(e, sub2(r, R)));     // FastTwoSum error (|R| > |e|)
+      R = r;
     }
-    const f2 sn = fma2(v, v, S);
-    const f2 e = fma2(v, v, sub2(S, sn));  // exact error of sn
-    S = sn;
-    const f2 r = add2(R, e);
-    T = add2(T, sub2(e, sub2(r, R)));     // FastTwoSum error (|R| > |e|)
-    R = r;
   }
   const float inv_u = exp2i(14 - 2 * E);
-  int cs = __float2int_rn(__fmul_rn(__fsub_rn(f2_lo(S), K2), inv_u)) +
-           __float2int_rn(__fmul_rn(__fsub_rn(f2_hi(S), K2), inv_u));
+  int cs_i = __float2int_rn(__fmul_rn(__fsub_rn(f2_lo(S), K2), inv_u)) +
+             __float2int_rn(__fmul_rn(__fsub_rn(f2_hi(S), K2), inv_u));
   const float inv_u2 = exp2i(32 - 2 * E);
   int cr = __float2int_rn(__fmul_rn(__fsub_rn(f2_lo(R), K3), inv_u2)) +
            __float2int_rn(__fmul_rn(__fsub_rn(f2_hi(R), K3), inv_u2));
   float t = __fadd_rn(f2_lo(T), f2_hi(T));
 #pragma unroll
   for (int o = 1; o < 4; o <<= 1) {
-    cs += __shfl_xor_sync(0xFFFFFFFFu, cs, o);
+    cs_i += __shfl_xor_sync(0xFFFFFFFFu, cs_i, o);
     cr += __shfl_xor_sync(0xFFFFFFFFu, cr, o);
     t = __fadd_rn(t, __shfl_xor_sync(0xFFFFFFFFu, t, o));
   }
-  dd sum = dd_add(int_to_dd(cs, exp2i(2 * E - 14)), int_to_dd(cr, exp2i(2 * E - 32)));
+  dd sum = dd_add(int_to_dd(cs_i, exp2i(2 * E - 14)), int_to_dd(cr, exp2i(2 * E - 32)));
   sum = dd_add(sum, dd{t, 0.0f});
   const dd ms = dd{__fmul_rn(sum.hi, 1.0f / kHeadDim), __fmul_rn(sum.lo, 1.0f / kHeadDim)};
-  return dd_rsqrt(dd_add(ms, dd{eps, 0.0f}));
+  const dd rr = dd_rsqrt(dd_add(ms, dd{eps, 0.0f}));
+  const f2 rh = f2_make(rr.hi, rr.hi);
+  // per chunk: n = RN_bf16(p r) (fast value within 1.5 ulps; the exact path where it may
+  // round the other way), then RoPE on the pairs and one 16-byte store
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float n[8];
+    bool unsure = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const f2 tt = mul2(p[4 * j + i], rh);
+      unsure |= near_bf16_midpoint(f2_lo(tt)) | near_bf16_midpoint(f2_hi(tt));
+      n[2 * i] = round_bf16(f2_lo(tt));
+      n[2 * i + 1] = round_bf16(f2_hi(tt));
+    }
+    if (unsure) {  // rare: redo the values whose fast value may round the other way
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float pv = (i & 1) ? f2_hi(p[4 * j + i / 2]) : f2_lo(p[4 * j + i / 2]);
+        if (near_bf16_midpoint(__fmul_rn(pv, rr.hi)))
+          n[i] = __uint_as_float(scaled_exact_bits(pv, rr.hi, rr.lo) << 16);
+      }
+    }
+    const float4 c4 = lds128(reinterpret_cast<const float4*>(cs + 4 * cidx[j]));
+    const float4 s4 = lds128(reinterpret_cast<const float4*>(cs + 64 + 4 * cidx[j]));
+    const float cv[4] = {c4.x, c4.y, c4.z, c4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = n[2 * i], b = n[2 * i + 1];
+      o[i] = pack_bf16x2(__fsub_rn(__fmul_rn(a, cv[i]), __fmul_rn(b, sv[i])),
+                         __fadd_rn(__fmul_rn(b, cv[i]), __fmul_rn(a, sv[i])));
+    }
+    if (live) __stcs(reinterpret_cast<uint4*>(dst + cidx[j] * 8), make_uint4(o[0], o[1], o[2], o[3]));
+  }
 }
 
-// Normalised words n = RN_bf16(x w r) for one packed word; sets `unsure` when the fast value
-// could round the other way (its low 16 bits lie within 3 of the BF16 midpoint pattern). The
-// fast value RN(p r_hi) (p = x w exact) is within 1.5 fp32 ulps of the exact p (r_hi + r_lo):
-// half an ulp from its rounding, under one from the neglected r_lo (|r_lo| <= 2^-24 r_hi).
-__device__ __forceinline__ uint32_t norm_word(f2 p, f2 rh, f2 rl, bool& unsure) {
-  (void)rl;
-  const f2 t = mul2(p, rh);
-  unsure |= near_bf16_midpoint(f2_lo(t)) | near_bf16_midpoint(f2_hi(t));
-  return pack_bf16x2(f2_lo(t), f2_hi(t));
-}
-
-__device__ __noinline__ uint32_t norm_word_exact(float p0, float p1, float r_hi, float r_lo) {
-  return scaled_exact_bits(p0, r_hi, r_lo) | (scaled_exact_bits(p1, r_hi, r_lo) << 16);
-}
-
-__device__ __forceinline__ uint32_t rope_word(uint32_t nw, float c, float s) {
-  const float a = bf_lo(nw), b = bf_hi(nw);
-  return pack_bf16x2(__fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)),
-                     __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, s)));
-}
-
-// Each warp runs its own pipeline over a flat list of work items, `kQkvDepth - 1` items
-// ahead, with no CTA-wide barrier after the start: item = (token, type), type one of the
-// eight-head blocks of Q, of K or of V. A Q/K item brings 2 KB of values (planar) and the
-// token's cos/sin row into the warp's slot; a V item brings 2 KB that go straight back out.
-// Type of the item with remainder r < 3 * octs (r / octs, by comparison: no division).
-__device__ __forceinline__ int item_type(int r, int octs) {
-  return int(r >= octs) + int(r >= 2 * octs);
-}
-
-constexpr int kQkvDepth = 4;           // slots per warp
-constexpr int kQkvWeightBytes = 2048;  // four fp32 RMSNorm weight vectors
-constexpr int kQkvSlotBytes = 2560;    // 8 heads x 256 B + cos/sin 512 B
-
-__global__ void __launch_bounds__(kQkvRingWarps * 32) qkv_ring_kernel(QkvParams P) {
-  extern __shared__ __align__(16) uint8_t qkv_smem[];
+__global__ void __launch_bounds__(kQwsThreads, 1) qkv_ws_kernel(QkvParams P, int S) {
+  extern __shared__ __align__(128) uint8_t qws_smem[];
   const int H = P.heads;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g8 = lane >> 2, qtr = lane & 3;
-  const int octs = (H + 7) >> 3;
-  const int per_token = 3 * octs;
-  const int64_t row_len = int64_t(H) * kHeadDim;
-  uint8_t* wsm = qkv_smem;
-  uint8_t* ring = qkv_smem + kQkvWeightBytes + warp * (kQkvDepth * kQkvSlotBytes);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int RB = H * 256;                          // bytes of one q, k or v row
+  const int stage_bytes = int(qws_stage_bytes(H));
+  float* wsm = reinterpret_cast<float*>(qws_smem);  // [4][128]: text q, k, image q, k
+  uint8_t* ring = qws_smem + kQkvWeightBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + size_t(S) * stage_bytes);
+  uint64_t* empty = full + S;
+  int* rowid = reinterpret_cast<int*>(empty + S);
+  int* next_unit = rowid + S;
+  const int64_t total = P.txt.tokens + P.img.tokens;
+  const int64_t t0 = total * blockIdx.x / gridDim.x;
+  const int n = int(total * (blockIdx.x + 1) / gridDim.x - t0);
+  if (n <= 0) return;  // uniform across the CTA
+  const int nq = (H + 7) >> 3;  // blocks of eight heads per Q or K row
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 2 * nq + 1);
+      rowid[s] = -1;
+    }
+    *next_unit = 0;
+    fence_mbar_init();
+  }
   wait_for_producers();
   allow_dependents();
-
-  // The four weight vectors as fp32, planar: 16-byte chunk c (values 4c .. 4c+3) of the
-  // 32-value quarter q at c * 64 + q * 16 (a stream without tokens has none).
-  for (int t = tid; t < 4 * 64; t += kQkvRingWarps * 32) {
-    const int w = t >> 6, pi = t & 63;  // vector, value pair
+  for (int t = threadIdx.x; t < 4 * 128; t += kQwsThreads) {
+    const int w = t >> 7, i = t & 127;
     const uint16_t* src = w == 0 ? P.txt.wq : w == 1 ? P.txt.wk : w == 2 ? P.img.wq : P.img.wk;
     const bool present = (w < 2 ? P.txt.tokens : P.img.tokens) > 0;
-    if (present) {
-      const uint32_t pair = __ldg(reinterpret_cast<const uint32_t*>(src) + pi);
-      const int q = pi >> 4, ii = pi & 15;
-      *reinterpret_cast<float2*>(wsm + w * 512 + (ii >> 1) * 64 + q * 16 + (ii & 1) * 8) =
-          make_float2(bf_lo(pair), bf_hi(pair));
-    }
+    wsm[t] = present ? __uint_as_float(uint32_t(__ldg(src + i)) << 16) : 0.0f;
   }
   __syncthreads();
+  const int64_t row_len = int64_t(H) * kHeadDim;
 
-  // Items gw, gw + W, gw + 2W, ... as (token, remainder) pairs, advanced without division.
-  struct Item {
-    int64_t token;
-    int r;     // 0 .. per_token - 1: type = r / octs, eight-head block = r % octs
-  };
-  const int64_t gw = int64_t(blockIdx.x) * kQkvRingWarps + warp;
-  const int64_t W = int64_t(gridDim.x) * kQkvRingWarps;
-  const int64_t w_tok = W / per_token;
-  const int w_rem = int(W - w_tok * per_token);
-  auto advance = [&](Item& it) {
-    it.token += w_tok;
-    it.r += w_rem;
-    if (it.r >= per_token) {
-      it.r -= per_token;
-      ++it.token;
-    }
-  };
-  const int64_t total_tokens = P.txt.tokens + P.img.tokens;
-  auto issue = [&](const Item& it, int slot) {
-    const bool is_txt = it.token < P.txt.tokens;
-    auto sel = [is_txt](auto a, auto b) { return is_txt ? a : b; };
-    const int64_t row = is_txt ? it.token : it.token - P.txt.tokens;
-    const int type = item_type(it.r, octs), oc = it.r - type * octs;
-    const uint16_t* base = type == 0 ? sel(P.txt.q, P.img.q)
-                         : type == 1 ? sel(P.txt.k, P.img.k) : sel(P.txt.v, P.img.v);
-    const uint16_t* src = base + row * sel(P.txt.ld, P.img.ld) + oc * 8 * kHeadDim;
-    uint8_t* dst = ring + slot * kQkvSlotBytes;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int c = lane + 32 * k;          // 16-byte chunk of the 2 KB block
-      const int hh = c >> 4, c16 = c & 15;  // head in the block, chunk in the head
-      if (oc * 8 + hh < H) {
-        const int off = type == 2 ? c * 16 : (c16 & 3) * 512 + (hh * 4 + (c16 >> 2)) * 16;
-        cp_async16(dst + off, src + c * 8);
+  if (warp == kQwsProducerWarp) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int k = 0, s = 0, u = 0; k < n; ++k) {
+        if (u > 0 && !mbar_wait(empty + s, (u - 1) & 1)) {
+          report_device_error(kDevErrWaitTimeout);
+          break;
+        }
+        const int64_t tok = t0 + k;
+        const bool txt = tok < P.txt.tokens;
+        const QkvStream& st = txt ? P.txt : P.img;
+        const int64_t row = txt ? tok : tok - P.txt.tokens;
+        uint8_t* stg = ring + size_t(s) * stage_bytes;
+        ws_set_row(rowid + s, k);
+        mbar_arrive_expect_tx(full + s, uint32_t(3 * RB + 512));
+        bulk_load(stg, st.q + row * st.ld, RB, full + s);
+        bulk_load(stg + RB, st.k + row * st.ld, RB, full + s);
+        bulk_load(stg + 2 * RB, st.v + row * st.ld, RB, full + s);
+        bulk_load(stg + 3 * RB, st.cos_sin + row * kHeadDim, 512, full + s);
+        issued = k + 1;
+        if (++s == S) {
+          s = 0;
+          ++u;
+        }
+      }
+      // the last copy into each stage has landed before this warp returns (always true on
+      // the normal path, where every token is consumed; it matters only after a wait ran out)
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / S) * S;
+        if (!mbar_wait(full + s, (last / S) & 1)) report_device_error(kDevErrWaitTimeout);
       }
     }
-    if (type != 2) {  // cos (lanes 0..15) and sin (16..31), planar within each 256 bytes
-      const float* cs = sel(P.txt.cos_sin, P.img.cos_sin) + row * kHeadDim;
-      const int half = lane >> 4, k = lane & 15;
-      cp_async16(dst + 2048 + half * 256 + (k & 3) * 64 + (k >> 2) * 16, cs + lane * 4);
-    }
-  };
-
-  // the item being processed and the one being issued (kQkvDepth - 1 items ahead)
-  Item cur{gw / per_token, int(gw % per_token)};
-  Item ahead = cur;
-#pragma unroll
-  for (int k = 0; k < kQkvDepth - 1; ++k) {
-    if (ahead.token < total_tokens) issue(ahead, k);
-    cp_async_commit();
-    advance(ahead);
+    return;
   }
-  for (int64_t k = 0; cur.token < total_tokens; ++k, advance(cur)) {
-    if (ahead.token < total_tokens) issue(ahead, int((k + kQkvDepth - 1) % kQkvDepth));
-    cp_async_commit();
-    advance(ahead);
-    cp_async_wait<kQkvDepth - 1>();
+
+  if (warp == kQwsVWarp) {
+    if (lane == 0) {
+      int pend = -1;  // stage whose v store was issued last and is not yet released
+      for (int k = 0, s = 0, u = 0; k < n; ++k) {
+        if (!mbar_wait(full + s, u & 1)) {
+          report_device_error(kDevErrWaitTimeout);
+          break;
+        }
+        bulk_store(P.jv + (t0 + k) * row_len, ring + size_t(s) * stage_bytes + 2 * RB, RB);
+        bulk_commit();
+        if (pend >= 0) {
+          bulk_wait_read<1>();  // the previous token's v row has been read
+          mbar_arrive(empty + pend);
+        }
+        pend = s;
+        if (++s == S) {
+          s = 0;
+          ++u;
+        }
+      }
+      bulk_wait<0>();  // every store complete before the CTA can release shared memory
+      if (pend >= 0) mbar_arrive(empty + pend);
+    }
+    return;
+  }
+
+  // Q/K warps
+  const int g8 = lane >> 2, qtr = lane & 3, odd = g8 & 1;
+  const int cidx[4] = {qtr + 4 * odd, qtr + 4 * (1 ^ odd), qtr + 4 * (2 ^ odd),
+                       qtr + 4 * (3 ^ odd)};
+  const int upt = 2 * nq;
+  const int units = n * upt;
+  for (int v = ws_claim(next_unit); v < units; v = ws_claim(next_unit)) {
+    const int k = v / upt, rem = v - k * upt;
+    const int kind = rem >= nq ? 1 : 0, oc = rem - kind * nq;
+    const int s = k % S, u = k / S;
+    if (!ws_wait_row(full + s, rowid, s, k, u)) {
+      report_device_error(kDevErrWaitTimeout);
+      break;
+    }
+    const int64_t tok = t0 + k;
+    const bool txt = tok < P.txt.tokens;
+    const int h = oc * 8 + g8;
+    const uint8_t* stg = ring + size_t(s) * stage_bytes;
+    uint16_t* dst = (kind == 0 ? P.jq : P.jk) + tok * row_len + int64_t(h) * kHeadDim;
+    qws_head(stg + kind * RB + h * 256, wsm + ((txt ? 0 : 2) + kind) * 128,
+             reinterpret_cast<const float*>(stg + 3 * RB), txt ? P.txt.eps : P.img.eps, cidx,
+             h < H, dst);
     __syncwarp();
-    const uint8_t* sl = ring + int(k % kQkvDepth) * kQkvSlotBytes;
-    const Item it = cur;
-    const int type = item_type(it.r, octs), oc = it.r - type * octs;
-    const bool is_txt = it.token < P.txt.tokens;
-    if (type == 2) {
-      uint16_t* dst = P.jv + it.token * row_len + oc * 8 * kHeadDim;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int c = lane + 32 * kk;
-        if (oc * 8 + (c >> 4) < H)
-          st_global16(dst + c * 8, lds128(reinterpret_cast<const float4*>(sl + c * 16)));
-      }
-    } else {
-      const int h = oc * 8 + g8;
-      uint32_t x[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (h < H) {
-          lds_words4(sl + j * 512 + (g8 * 4 + qtr) * 16, x + 4 * j);
-        } else {
-          x[4 * j] = x[4 * j + 1] = x[4 * j + 2] = x[4 * j + 3] = 0u;
-        }
-      }
-      const uint8_t* wv = wsm + ((is_txt ? 0 : 2) + type) * 512 + qtr * 16;
-      f2 p[16];
-      const dd r = head_rrms4(x, wv, is_txt ? P.txt.eps : P.img.eps, p);
-      const f2 rh = f2_make(r.hi, r.hi), rl = f2_make(r.lo, r.lo);
-      uint32_t n[16];
-      bool unsure = false;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) n[i] = norm_word(p[i], rh, rl, unsure);
-      if (unsure) {  // rare: redo the words whose fast value may round the other way
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          bool u = false;
-          norm_word(p[i], rh, rl, u);
-          if (u) n[i] = norm_word_exact(f2_lo(p[i]), f2_hi(p[i]), r.hi, r.lo);
-        }
-      }
-      const uint8_t* csv = sl + 2048 + qtr * 16;
-      uint32_t o[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 c4 = lds128(reinterpret_cast<const float4*>(csv + j * 64));
-        const float4 s4 = lds128(reinterpret_cast<const float4*>(csv + 256 + j * 64));
-        o[4 * j + 0] = rope_word(n[4 * j + 0], c4.x, s4.x);
-        o[4 * j + 1] = rope_word(n[4 * j + 1], c4.y, s4.y);
-        o[4 * j + 2] = rope_word(n[4 * j + 2], c4.z, s4.z);
-        o[4 * j + 3] = rope_word(n[4 * j + 3], c4.w, s4.w);
-      }
-      if (h < H) {
-        uint16_t* dst = (type == 0 ? P.jq : P.jk) + it.token * row_len + h * kHeadDim + qtr * 32;
-        st_stream32(dst, *reinterpret_cast<const uint32_t(*)[8]>(o));
-        st_stream32(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(o + 8));
-      }
-    }
-    __syncwarp();  // every lane is done with the slot before it is refilled
+    if (lane == 0) mbar_arrive(empty + s);
   }
-  cp_async_wait<0>();
 }
-
 }  // namespace fp8q
