@@ -570,13 +570,15 @@ fp8q_status fp8q_qkv_epilogue(void* joint_q, void* joint_k, void* joint_v,
     const int stages = int(std::min<int64_t>(fit, fp8q::kQwsMaxStages));
     if (stages >= 2) {
       const size_t smem = fp8q::qws_smem_bytes(int(heads), stages);
-      auto* fn = fp8q::qkv_ws_kernel;
+      const int nw = fp8q::qws_qk_warps(int(heads));
+      auto* fn = nw == 16 ? fp8q::qkv_ws_kernel<16> : fp8q::qkv_ws_kernel<13>;
+      const int threads = fp8q::qws_threads(nw);
       int bps = 0;
-      stt = blocks_per_sm(reinterpret_cast<const void*>(fn), fp8q::kQwsThreads, smem, &bps);
+      stt = blocks_per_sm(reinterpret_cast<const void*>(fn), threads, smem, &bps);
       if (stt != FP8Q_OK) return stt;
       if (bps > 0) {
         const int64_t grid = std::min<int64_t>(total, dev->sms);
-        return launch(fn, dim3(unsigned(grid)), dim3(fp8q::kQwsThreads), smem, stream, p, stages);
+        return launch(fn, dim3(unsigned(grid)), dim3(threads), smem, stream, p, stages);
       }
     }
   }

@@ -274,11 +274,14 @@ __device__ __forceinline__ void lds_words4(const uint8_t* p, uint32_t* w) {
 // word, so it cannot take an older phase of the same parity for its own. The V warp and the
 // producer take the stage's uses in order. Every wait is bounded; a wait that runs out records
 // the device error and the warp stops.
-constexpr int kQwsQkWarps = 12;                  // Q/K warps per CTA
-constexpr int kQwsVWarp = kQwsQkWarps;           // then the V warp
-constexpr int kQwsProducerWarp = kQwsQkWarps + 1;
-constexpr int kQwsThreads = (kQwsQkWarps + 2) * 32;
+// Q/K warps per CTA (NW), then the V warp and the producer warp. Measured on GB300 (graph
+// replay of back-to-back launches, Qwen-Image 24 heads / FLUX.2 48 heads, microseconds):
+// 13 warps 31.8 / 57.9, 14: 31.3 / 59.1, 15: 30.9 / 59.7, 16: 30.7 / 60.2; so 16 up to 32
+// heads (18 warps: registers capped at 96, so that five warps fit a sub-partition's register
+// file) and 13 above.
 constexpr int kQwsMaxStages = 32;
+__host__ __device__ constexpr int qws_qk_warps(int heads) { return heads <= 32 ? 16 : 13; }
+__host__ __device__ constexpr int qws_threads(int nw) { return (nw + 2) * 32; }
 
 // Dynamic shared memory of the warp-specialised kernel: weights, S stages, then per stage two
 // mbarriers and the row word, and the unit counter.
@@ -379,15 +382,18 @@ __device__ __forceinline__ void qws_head(const uint8_t* xs, const float* wt, con
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float a = n[2 * i], b = n[2 * i + 1];
-      o[i] = pack_bf16x2(__fsub_rn(__fmul_rn(a, cv[i]), __fmul_rn(b, sv[i])),
-                         __fadd_rn(__fmul_rn(b, cv[i]), __fmul_rn(a, sv[i])));
+      // products on both lanes at once, sums as separate roundings (no fused operation)
+      const f2 ab = f2_make(n[2 * i], n[2 * i + 1]);
+      const f2 pc = mul2(ab, f2_make(cv[i], cv[i])), ps = mul2(ab, f2_make(sv[i], sv[i]));
+      o[i] = pack_bf16x2(__fsub_rn(f2_lo(pc), f2_hi(ps)), __fadd_rn(f2_hi(pc), f2_lo(ps)));
     }
     if (live) __stcs(reinterpret_cast<uint4*>(dst + cidx[j] * 8), make_uint4(o[0], o[1], o[2], o[3]));
   }
 }
 
-__global__ void __launch_bounds__(kQwsThreads, 1) qkv_ws_kernel(QkvParams P, int S) {
+template <int NW>
+__global__ void __maxnreg__(NW + 2 > 16 ? 96 : 128) qkv_ws_kernel(QkvParams P, int S) {
+  constexpr int kVWarp = NW, kProducerWarp = NW + 1, kThreads = qws_threads(NW);
   extern __shared__ __align__(128) uint8_t qws_smem[];
   const int H = P.heads;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -415,7 +421,7 @@ __global__ void __launch_bounds__(kQwsThreads, 1) qkv_ws_kernel(QkvParams P, int
   }
   wait_for_producers();
   allow_dependents();
-  for (int t = threadIdx.x; t < 4 * 128; t += kQwsThreads) {
+  for (int t = threadIdx.x; t < 4 * 128; t += kThreads) {
     const int w = t >> 7, i = t & 127;
     const uint16_t* src = w == 0 ? P.txt.wq : w == 1 ? P.txt.wk : w == 2 ? P.img.wq : P.img.wk;
     const bool present = (w < 2 ? P.txt.tokens : P.img.tokens) > 0;
@@ -424,7 +430,7 @@ __global__ void __launch_bounds__(kQwsThreads, 1) qkv_ws_kernel(QkvParams P, int
   __syncthreads();
   const int64_t row_len = int64_t(H) * kHeadDim;
 
-  if (warp == kQwsProducerWarp) {
+  if (warp == kProducerWarp) {
     if (lane == 0) {
       int issued = 0;
       for (int k = 0, s = 0, u = 0; k < n; ++k) {
@@ -459,7 +465,7 @@ __global__ void __launch_bounds__(kQwsThreads, 1) qkv_ws_kernel(QkvParams P, int
     return;
   }
 
-  if (warp == kQwsVWarp) {
+  if (warp == kVWarp) {
     if (lane == 0) {
       int pend = -1;  // stage whose v store was issued last and is not yet released
       for (int k = 0, s = 0, u = 0; k < n; ++k) {
