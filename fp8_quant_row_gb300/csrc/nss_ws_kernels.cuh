@@ -116,9 +116,11 @@ __device__ __forceinline__ uint4 ws_fix_uncertain8(const uint4 x, const uint4 n,
 }
 
 // y and q of one 768-column part of a row: this lane's chunks are xs[j * 32] (shared memory),
-// its RN(1 + scale) and shift pairs ops[j][i], sh[j][i] (registers). The per-element
-// |t| < t_small test is always made (one code path; t_small is zero unless the row's mean
-// lies close to a bf16 value, where the absolute error of t matters).
+// its RN(1 + scale) and shift pairs ops[j][i], sh[j][i] (registers). kSmall adds the
+// per-element |t| < t_small test; t_small is zero unless the row's mean lies close to a bf16
+// value (where the absolute error of t matters), so the body without the test serves almost
+// every row (the choice is per row and uniform across the warp).
+template <bool kSmall>
 __device__ __forceinline__ void ws_part_outputs(const uint4* xs, const f2 (&ops)[kWsPartChunks][4],
                                                 const f2 (&sh)[kWsPartChunks][4],
                                                 const RowConst& kc, f2 inv2, uint4* yr,
@@ -136,7 +138,7 @@ __device__ __forceinline__ void ws_part_outputs(const uint4* xs, const f2 (&ops)
       const f2 tt = fma2(sub2(bf2_to_f2(w4[i]), mu2), r2, c2);
       const float t0 = f2_lo(tt), t1 = f2_hi(tt);
       any |= near_bf16_midpoint(t0) | near_bf16_midpoint(t1);
-      any |= (fabsf(t0) < kc.t_small) | (fabsf(t1) < kc.t_small);
+      if (kSmall) any |= (fabsf(t0) < kc.t_small) | (fabsf(t1) < kc.t_small);
       n[2 * i] = round_bf16(t0);
       n[2 * i + 1] = round_bf16(t1);
     }
@@ -298,7 +300,10 @@ __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
     const size_t off = size_t(blk.begin + k) * C + col0;
     uint4* yr = reinterpret_cast<uint4*>(p.y + off) + lane;
     uint2* qr = reinterpret_cast<uint2*>(p.q + off) + lane;
-    ws_part_outputs(xs, ops, sh, kc, inv2, yr, qr);
+    if (kc.t_small != 0.0f)
+      ws_part_outputs<true>(xs, ops, sh, kc, inv2, yr, qr);
+    else
+      ws_part_outputs<false>(xs, ops, sh, kc, inv2, yr, qr);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + s);
   }

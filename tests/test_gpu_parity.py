@@ -215,6 +215,49 @@ def test_nss_value_range_edges(cols):
             check_ln(yg, qg, yr, qr, s, f"value-range edges {x.shape[0]}x{cols} s={s}")
 
 
+def _mean_on_grid_rows(cols, rng):
+    """Rows whose mean lies within 2^-18 |mean| of a bf16 value c while most elements equal c,
+    so x - mean is tiny and the per-element |t| < t_small test (exact path) decides: cols - 2
+    elements c, one 2c and one c * 2^-20 (mean c (1 + 2^-20 / cols)), for several c and signs;
+    also c with five elements a step above and ten half a step below (mean c where the steps
+    are bf16 values)."""
+    bf = lambda v: W.to_bf16_bits(torch.tensor(np.asarray(v, np.float32)))
+    rows = []
+    for c in (1.0, -3.0, 0.75 * 2.0 ** 40, -1.5 * 2.0 ** -30, 100.0):
+        r = np.full(cols, c)
+        idx = rng.permutation(cols)
+        r[idx[0]] = 2 * c
+        r[idx[1]] = c * 2.0 ** -20
+        rows.append(bf(r))
+        r = np.full(cols, c)
+        step = abs(c) * 2.0 ** -7
+        r[idx[:5]] += step
+        r[idx[5:15]] -= step / 2
+        rows.append(bf(r))
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("cols", (3072, 6144))
+def test_nss_mean_on_a_bf16_value(cols):
+    """Rows that take the per-element |t| < t_small exact path, alone and inside a launch large
+    enough for the tuned kernels (width 3072: warp-specialised, whose output warps pick the
+    code path with that test per row; 6144: two warps per row)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rng = np.random.default_rng(cols + 7)
+    special = _mean_on_grid_rows(cols, rng)
+    g = torch.Generator().manual_seed(cols + 7)
+    scale = W.normal_bf16((1, cols), 0.1, g)
+    shift = W.normal_bf16((1, cols), 0.1, g)
+    big = W.nss_inputs(2 * sms + 101, cols, seed=cols + 8)["x"]
+    big[5::29][: len(special) * 3] = np.tile(special, (3, 1))[: big[5::29].shape[0]]
+    for x in (special, big):
+        for s in (0.05, 3.0):
+            inp = dict(x=x, scale=scale, shift=shift)
+            yg, qg = run_nss(inp, s)
+            yr, qr = oracle.nss_fp8(x, scale, shift, s)
+            check_ln(yg, qg, yr, qr, s, f"mean on a bf16 value {x.shape[0]}x{cols} s={s}")
+
+
 def test_nss_row_pieces_reproduce_the_single_call():
     """A FLUX.2-shaped launch (two modulation groups) cut for 3 and 8 ranks into pieces that
     lie inside one group (each a call with mod_rows = 0 and its group's scale/shift rows):
@@ -287,6 +330,61 @@ def test_pdl_producer_consumer_chains_on_one_stream():
                                        (y4, q4, y1_ref, q1_ref, "after a torch copy")):
             check_ln(G.host_u16(yg), G.host_u8(qg), yr_, qr_, s, f"PDL chain {what} rep {rep}")
         assert np.array_equal(G.host_u8(qc), qc_ref), f"rep {rep}: token_cat after a torch copy"
+
+
+def test_pdl_chains_qkv_and_nvfp4_on_one_stream():
+    """As above for the warp-specialised QKV epilogue and token_cat_nvfp4, on one stream with
+    no synchronisation in between: a torch elementwise kernel writes the packed QKV rows ->
+    qkv_epilogue -> a second qkv_epilogue whose q, k, v are the first one's outputs; a torch
+    elementwise kernel writes the attention part -> token_cat_nvfp4. The oracle's composition
+    is the reference."""
+    H, tt, it = 24, 64, 300
+    d = W.qkv_inputs(tt, it, H, seed=7)
+    T = tt + it
+    r1 = oracle.qkv_epilogue(d["txt"], d["img"], H)
+
+    def second(lo, hi, st, arrs):
+        return dict(q=arrs[0][lo:hi].reshape(hi - lo, H * 128),
+                    k=arrs[1][lo:hi].reshape(hi - lo, H * 128),
+                    v=arrs[2][lo:hi].reshape(hi - lo, H * 128),
+                    wq=st["wq"], wk=st["wk"], cos_sin=st["cos_sin"], eps=st["eps"])
+
+    r2 = oracle.qkv_epilogue(second(0, tt, d["txt"], r1), second(tt, T, d["img"], r1), H)
+    srcs = {k: G.dev_bf16(d[k]["packed"]) for k in ("txt", "img")}
+    c = W.CONFIGS["token_cat_nvfp4_flux"]
+    t = W.config_inputs("token_cat_nvfp4_flux")
+    rows = 512
+    qn_ref, sn_ref = oracle.token_cat_nvfp4(t["a"][:rows], t["m"][:rows], c["global_scale"])
+    a_src, m = G.dev_bf16(t["a"][:rows]), G.dev_bf16(t["m"][:rows])
+    a = torch.zeros_like(a_src)
+    gs = G.dev_scale(c["global_scale"])
+    for rep in range(3):
+        packed = {k: torch.zeros_like(v) for k, v in srcs.items()}
+        torch.cuda.synchronize()
+        for k in packed:
+            torch.mul(srcs[k], 1, out=packed[k])  # an elementwise torch kernel as the producer
+        o1 = fq().qkv_epilogue(_dev_stream(d["txt"], H, packed["txt"]),
+                               _dev_stream(d["img"], H, packed["img"]), H)
+
+        def dev_second(lo, hi, st):
+            return dict(q=o1[0][lo:hi].view(hi - lo, H * 128), k=o1[1][lo:hi].view(hi - lo, H * 128),
+                        v=o1[2][lo:hi].view(hi - lo, H * 128), q_weight=G.dev_bf16(st["wq"]),
+                        k_weight=G.dev_bf16(st["wk"]),
+                        cos_sin=torch.from_numpy(st["cos_sin"]).cuda(), eps=st["eps"])
+
+        txt2, img2 = dev_second(0, tt, d["txt"]), dev_second(tt, T, d["img"])
+        o2 = fq().qkv_epilogue(txt2, img2, H)
+        a.zero_()
+        torch.mul(a_src, 1, out=a)
+        qn, sn = fq().token_cat_nvfp4(a, m, gs)
+        torch.cuda.synchronize()
+        assert fq().device_error() == 0, f"rep {rep}: a bounded wait inside a kernel ran out"
+        for name, got, ref in zip("qkv", o1, r1):
+            assert np.array_equal(G.host_u16(got), ref), f"rep {rep}: first qkv {name}"
+        for name, got, ref in zip("qkv", o2, r2):
+            assert np.array_equal(G.host_u16(got), ref), f"rep {rep}: chained qkv {name}"
+        assert np.array_equal(G.host_u8(qn), qn_ref), f"rep {rep}: token_cat_nvfp4 codes"
+        assert np.array_equal(G.host_u8(sn), sn_ref), f"rep {rep}: token_cat_nvfp4 scales"
 
 
 def test_nss_eps_values():
