@@ -486,6 +486,20 @@ __device__ __forceinline__ bool ws_wait_row(uint64_t* bar, const int* rowid, int
 
 // Four E4M3 codes E4M3(RN(y * inv)) of two bf16 pairs, as one 32-bit word (y0 low pair in
 // bytes 0-1, y1 in bytes 2-3): two packed multiplies, two conversions, one byte permute.
+// Four E4M3 codes of the y values already rounded to bf16 and held as fp32 pairs (as quant4,
+// without unpacking packed words).
+__device__ __forceinline__ uint32_t quant4f(f2 y0, f2 y1, f2 inv2) {
+  const f2 a = mul2(y0, inv2), b = mul2(y1, inv2);
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t.reg .f32 a0, a1, b0, b1;\n\t"
+      "mov.b64 {a0, a1}, %1;\n\tmov.b64 {b0, b1}, %2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, a1, a0;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, b1, b0;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "l"(a.v), "l"(b.v));
+  return r;
+}
 __device__ __forceinline__ uint32_t quant4(uint32_t y0, uint32_t y1, unsigned long long inv2) {
   unsigned long long a, b;
   asm("{\n\t.reg .b64 v;\n\tmov.b64 v, {%1, %2};\n\tmul.rn.f32x2 %0, v, %3;\n\t}"

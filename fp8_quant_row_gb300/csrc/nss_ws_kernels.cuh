@@ -154,13 +154,16 @@ __device__ __forceinline__ void ws_part_outputs(const uint4* xs, const f2 (&ops)
       }
     }
     uint32_t yw[4];
+    f2 yb[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const f2 yf = fma2(f2_make(n[2 * i], n[2 * i + 1]), ops[j][i], sh[j][i]);
-      yw[i] = pack_bf16x2(f2_lo(yf), f2_hi(yf));
+      // y rounded to bf16 as fp32 values (for q), and the same values packed (for y)
+      yb[i] = f2_make(round_bf16(f2_lo(yf)), round_bf16(f2_hi(yf)));
+      yw[i] = __byte_perm(__float_as_uint(f2_lo(yb[i])), __float_as_uint(f2_hi(yb[i])), 0x7632);
     }
     st_stream(yr + j * 32, make_uint4(yw[0], yw[1], yw[2], yw[3]));
-    st_stream(qr + j * 32, make_uint2(quant4(yw[0], yw[1], inv2.v), quant4(yw[2], yw[3], inv2.v)));
+    st_stream(qr + j * 32, make_uint2(quant4f(yb[0], yb[1], inv2), quant4f(yb[2], yb[3], inv2)));
   }
 }
 
