@@ -667,6 +667,14 @@ def test_qkv_epilogue_shapes(tt, it, heads, extra):
     check_qkv(d, heads, f"{tt}+{it}x{heads}")
 
 
+@pytest.mark.parametrize("tt,it,heads", [(300, 1700, 64), (100, 6000, 1), (50, 2000, 33)])
+def test_qkv_epilogue_stage_reuse(tt, it, heads):
+    """Enough tokens per CTA that every stage of the warp-specialised kernel's ring is reused
+    several times: 64 heads (4 stages of 48.5 KB, 13 tokens per CTA), 1 head (32 stages,
+    ~40 tokens per CTA), 33 heads (the 13-warp variant, a partial block of eight heads)."""
+    check_qkv(W.qkv_inputs(tt, it, heads, seed=heads + 101), heads, f"reuse {tt}+{it}x{heads}")
+
+
 def test_qkv_epilogue_special_heads():
     """Zero heads, constant heads, tiny and huge magnitudes, exact midpoint products,
     right-angle and identity rotations."""
