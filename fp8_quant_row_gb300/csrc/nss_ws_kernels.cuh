@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
     return;
   }
 
+  int part;
   if (warp < NS) {
     // statistics warp
     const float colsf = float(C);
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
       const int s = k & (S - 1), u = k >> L::kLogStages;
       if (!ws_wait_row(full + s, rowid, s, k, u)) {
         report_device_error(kDevErrWaitTimeout);
-        break;
+        return;
       }
       const uint4* stage = reinterpret_cast<const uint4*>(ring + size_t(s) * L::kRowBytes) + lane;
       const RowConst kc = ws_row_stats<L::kStatsChunks>(stage, colsf, rcols, p.eps);
@@ -258,11 +259,15 @@ __global__ void __launch_bounds__(WsLayout<C, NS, NO>::kThreads, 1)
         mbar_arrive(done + s);
       }
     }
-    return;
+    // No row is left for the statistics role (the end of the CTA's rows): the warp joins the
+    // output warps of part warp % P, whose rows still wait there, and takes rows from the same
+    // counter, so every part-row is still written once.
+    part = warp % P;
+  } else {
+    part = (warp - NS) % P;
   }
 
   // output warp: part `part` of the rows it claims
-  const int part = (warp - NS) % P;
   const size_t col0 = size_t(part) * kWsPartCols;
   f2 ops[kWsPartChunks][4], sh[kWsPartChunks][4];
   {
