@@ -31,6 +31,10 @@
 // use has been released, so every earlier phase of its barriers has completed and the parity
 // cannot be mistaken for an older phase's.
 //
+// A statistics warp that finds no row left joins the output warps of one part (the same
+// per-part claim counter), so the last rows' outputs, which end the CTA, are shared among more
+// warps (the producer warp joining as well, once every row is issued, was slower).
+//
 // Every wait is bounded (kWaitLimitCycles); a wait that runs out records kDevErrWaitTimeout
 // in the device error word and the warp stops taking rows. The producer finally waits
 // (bounded) for its own copies still in flight before it returns.
