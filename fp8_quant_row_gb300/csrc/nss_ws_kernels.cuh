@@ -20,7 +20,7 @@
 //
 // The constants of a row are formed once (not once per warp that touches the row), the
 // statistics (FMA-pipe heavy) and output (ALU heavy) phases of different rows run at the same
-// time on different warps, no consumer warp ever issues a load from global memory, and a row
+// time on different warps, no consumer warp loads row data from global memory, and a row
 // goes to whichever warp of a role is free first (a static row-to-warp assignment made rows
 // wait for one busy warp while others idled).
 //

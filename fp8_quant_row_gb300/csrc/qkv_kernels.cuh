@@ -266,7 +266,8 @@ __device__ __forceinline__ void lds_words4(const uint8_t* p, uint32_t* w) {
 // Four lanes per head, 32 values per lane: lane q of a head holds the 16-byte chunks
 // c = q + 4 (j ^ o), j = 0..3, o the parity of the head within the block, so that one
 // 16-byte load of chunk index j by the warp reads 64 contiguous bytes per head and the eight
-// heads split evenly over the two halves of the banks (no conflicts). Values 8c .. 8c + 7 of
+// heads split evenly over the two halves of the banks (value loads without conflicts; the
+// weight loads of chunks c and c + 4 share banks, two ways). Values 8c .. 8c + 7 of
 // chunk c are RoPE pairs 4c .. 4c + 3.
 // mbarrier phases: stage s = k % S holds tokens s, s + S, ...; token k waits for the phase of
 // parity (k / S) & 1. The producer writes k into the stage's row word (release) before it
