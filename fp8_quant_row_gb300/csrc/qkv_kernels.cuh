@@ -237,7 +237,11 @@ __global__ void __launch_bounds__(kQkvWarps * 32, kQkvMinCtas) qkv_epilogue_kern
 // ------------------------------------------------------------------------------------------
 
 constexpr int kQkvMaxWsHeads = 64;     // the warp-specialised kernel's head limit
-constexpr int kQkvWeightBytes = 2048;  // four fp32 RMSNorm weight vectors
+// The four fp32 RMSNorm weight vectors (text q, k, image q, k), each 140 floats: the 8 weights
+// of chunk c at 8c + 4 (c / 4), so that the lanes reading chunks c and c + 4 (the two head
+// parities of a step) hit different banks.
+constexpr int kQkvWeightStride = 140;
+constexpr int kQkvWeightBytes = 4 * kQkvWeightStride * 4;
 
 __device__ __forceinline__ void lds_words4(const uint8_t* p, uint32_t* w) {
   const float4 v = lds128(reinterpret_cast<const float4*>(p));
@@ -266,8 +270,8 @@ __device__ __forceinline__ void lds_words4(const uint8_t* p, uint32_t* w) {
 // Four lanes per head, 32 values per lane: lane q of a head holds the 16-byte chunks
 // c = q + 4 (j ^ o), j = 0..3, o the parity of the head within the block, so that one
 // 16-byte load of chunk index j by the warp reads 64 contiguous bytes per head and the eight
-// heads split evenly over the two halves of the banks (value loads without conflicts; the
-// weight loads of chunks c and c + 4 share banks, two ways). Values 8c .. 8c + 7 of
+// heads split evenly over the two halves of the banks (no conflicts; the weight table is padded
+// for the same reason, see kQkvWeightStride). Values 8c .. 8c + 7 of
 // chunk c are RoPE pairs 4c .. 4c + 3.
 // mbarrier phases: stage s = k % S holds tokens s, s + S, ...; token k waits for the phase of
 // parity (k / S) & 1. The producer writes k into the stage's row word (release) before it
@@ -294,7 +298,7 @@ __host__ __device__ constexpr size_t qws_smem_bytes(int heads, int stages) {
 }
 
 // RMSNorm + interleaved RoPE of the 16 words this lane holds, written to `dst` (the head's
-// output row). xs: the head's 256 bytes in the stage; wt: the 128 fp32 weights; cs: the
+// output row). xs: the head's 256 bytes in the stage; wt: the padded fp32 weights; cs: the
 // stage's cos (64 fp32) and sin (64 fp32) row; cidx: the lane's four chunk indices.
 __device__ __forceinline__ void qws_head(const uint8_t* xs, const float* wt, const float* cs,
                                          float eps, const int (&cidx)[4], bool live,
@@ -322,8 +326,9 @@ __device__ __forceinline__ void qws_head(const uint8_t* xs, const float* wt, con
   f2 p[16];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float4 w0 = lds128(reinterpret_cast<const float4*>(wt + 8 * cidx[j]));
-    const float4 w1 = lds128(reinterpret_cast<const float4*>(wt + 8 * cidx[j] + 4));
+    const float* wc = wt + 8 * cidx[j] + 4 * (cidx[j] >> 2);
+    const float4 w0 = lds128(reinterpret_cast<const float4*>(wc));
+    const float4 w1 = lds128(reinterpret_cast<const float4*>(wc + 4));
     const f2 wp[4] = {f2_make(w0.x, w0.y), f2_make(w0.z, w0.w), f2_make(w1.x, w1.y),
                       f2_make(w1.z, w1.w)};
 #pragma unroll
@@ -400,7 +405,7 @@ __global__ void __maxnreg__(NW + 2 > 16 ? 96 : 128) qkv_ws_kernel(QkvParams P, i
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int RB = H * 256;                          // bytes of one q, k or v row
   const int stage_bytes = int(qws_stage_bytes(H));
-  float* wsm = reinterpret_cast<float*>(qws_smem);  // [4][128]: text q, k, image q, k
+  float* wsm = reinterpret_cast<float*>(qws_smem);  // [4][kQkvWeightStride]: text q, k, image q, k
   uint8_t* ring = qws_smem + kQkvWeightBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + size_t(S) * stage_bytes);
   uint64_t* empty = full + S;
@@ -426,7 +431,8 @@ __global__ void __maxnreg__(NW + 2 > 16 ? 96 : 128) qkv_ws_kernel(QkvParams P, i
     const int w = t >> 7, i = t & 127;
     const uint16_t* src = w == 0 ? P.txt.wq : w == 1 ? P.txt.wk : w == 2 ? P.img.wq : P.img.wk;
     const bool present = (w < 2 ? P.txt.tokens : P.img.tokens) > 0;
-    wsm[t] = present ? __uint_as_float(uint32_t(__ldg(src + i)) << 16) : 0.0f;
+    wsm[w * kQkvWeightStride + i + 4 * (i >> 5)] =
+        present ? __uint_as_float(uint32_t(__ldg(src + i)) << 16) : 0.0f;
   }
   __syncthreads();
   const int64_t row_len = int64_t(H) * kHeadDim;
@@ -511,7 +517,7 @@ __global__ void __maxnreg__(NW + 2 > 16 ? 96 : 128) qkv_ws_kernel(QkvParams P, i
     const int h = oc * 8 + g8;
     const uint8_t* stg = ring + size_t(s) * stage_bytes;
     uint16_t* dst = (kind == 0 ? P.jq : P.jk) + tok * row_len + int64_t(h) * kHeadDim;
-    qws_head(stg + kind * RB + h * 256, wsm + ((txt ? 0 : 2) + kind) * 128,
+    qws_head(stg + kind * RB + h * 256, wsm + ((txt ? 0 : 2) + kind) * kQkvWeightStride,
              reinterpret_cast<const float*>(stg + 3 * RB), txt ? P.txt.eps : P.img.eps, cidx,
              h < H, dst);
     __syncwarp();
